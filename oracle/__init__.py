@@ -1,0 +1,230 @@
+"""Double-precision CPU oracle for the fused gated activation (test infrastructure).
+
+This package exists to check the CUDA library; it is NOT part of the product
+path.  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import it.  It shares no code with the CUDA library and never
+imports it.
+
+The arithmetic lives in ``glu_oracle.c`` (plain C, double precision, one RNE
+rounding into the storage dtype).  This module compiles it with gcc, loads it
+with ctypes, and restates the two operand layouts of the page
+"Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel" (Inputs the agent should
+gather first, item 4): separate ``a``/``b`` tensors, or one tensor ``x`` whose
+row holds ``[gate | up]`` with ``a = x[:, :I]`` and ``b = x[:, I:2I]``.
+
+Arrays are numpy arrays of raw bit patterns: ``uint32`` for f32, ``uint16`` for
+f16 and bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "glu_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_glu.so")
+
+ACTS = {"silu": 0, "gelu_erf": 1, "gelu_tanh": 2, "relu": 3}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+BITS_DTYPE = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, IEEE semantics: no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+            ci = ctypes.c_int
+            L.oracle_fwd.argtypes = [ci, ci, vp, vp, vp, i64]
+            L.oracle_bwd.argtypes = [ci, ci, vp, vp, vp, vp, vp, i64]
+            L.oracle_bwd_da_scale.argtypes = [ci, ci, vp, vp, vp, dp, i64]
+            L.oracle_act_vec.argtypes = [ci, dp, dp, i64]
+            L.oracle_act_grad_terms_vec.argtypes = [ci, dp, dp, dp, i64]
+            L.oracle_round_vec.argtypes = [ci, dp, dp, i64]
+            L.oracle_encode_vec.argtypes = [ci, dp, vp, i64]
+            L.oracle_decode_vec.argtypes = [ci, vp, dp, i64]
+            L.oracle_sigmoid.argtypes = [ctypes.c_double]
+            L.oracle_sigmoid.restype = ctypes.c_double
+            for f in (L.oracle_fwd, L.oracle_bwd, L.oracle_bwd_da_scale, L.oracle_act_vec,
+                      L.oracle_act_grad_terms_vec, L.oracle_round_vec, L.oracle_encode_vec,
+                      L.oracle_decode_vec):
+                f.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(x: np.ndarray) -> int:
+    return x.ctypes.data
+
+
+def _bits(x, dtype: str) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=BITS_DTYPE[dtype])
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+# ---- scalar maps over doubles -------------------------------------------------
+
+def sigmoid(x: float) -> float:
+    return lib().oracle_sigmoid(float(x))
+
+
+def act(name: str, x) -> np.ndarray:
+    """act(x) in double, no rounding."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    lib().oracle_act_vec(ACTS[name], _ptr(x), _ptr(out), x.size)
+    return out
+
+
+def act_grad_terms(name: str, x):
+    """The two terms whose sum is act'(x) (see glu_oracle.c)."""
+    x = _f64(x)
+    t1, t2 = np.empty_like(x), np.empty_like(x)
+    lib().oracle_act_grad_terms_vec(ACTS[name], _ptr(x), _ptr(t1), _ptr(t2), x.size)
+    return t1, t2
+
+
+def act_grad(name: str, x) -> np.ndarray:
+    t1, t2 = act_grad_terms(name, x)
+    return t1 + t2
+
+
+def round_to(dtype: str, x) -> np.ndarray:
+    """Round doubles to the nearest value of ``dtype`` (ties to even)."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    lib().oracle_round_vec(DTYPES[dtype], _ptr(x), _ptr(out), x.size)
+    return out
+
+
+def encode(dtype: str, x) -> np.ndarray:
+    x = _f64(x)
+    out = np.empty(x.shape, dtype=BITS_DTYPE[dtype])
+    lib().oracle_encode_vec(DTYPES[dtype], _ptr(x), _ptr(out), x.size)
+    return out
+
+
+def decode(dtype: str, bits) -> np.ndarray:
+    bits = _bits(bits, dtype)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib().oracle_decode_vec(DTYPES[dtype], _ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+# ---- element-wise forward / backward over bit arrays --------------------------
+
+def fwd(act_name: str, dtype: str, a, b) -> np.ndarray:
+    """y = round(act(a) * b), element by element; a and b have one shape."""
+    a, b = _bits(a, dtype), _bits(b, dtype)
+    if a.shape != b.shape:
+        raise ValueError("a and b must have the same shape")
+    y = np.empty_like(a)
+    lib().oracle_fwd(ACTS[act_name], DTYPES[dtype], _ptr(a), _ptr(b), _ptr(y), a.size)
+    return y
+
+
+def bwd(act_name: str, dtype: str, dc, a, b):
+    """(da, db) = (round(dc * act'(a) * b), round(dc * act(a)))."""
+    dc, a, b = _bits(dc, dtype), _bits(a, dtype), _bits(b, dtype)
+    if not (a.shape == b.shape == dc.shape):
+        raise ValueError("dc, a and b must have the same shape")
+    da, db = np.empty_like(a), np.empty_like(a)
+    lib().oracle_bwd(ACTS[act_name], DTYPES[dtype], _ptr(dc), _ptr(a), _ptr(b),
+                     _ptr(da), _ptr(db), a.size)
+    return da, db
+
+
+def bwd_da_scale(act_name: str, dtype: str, dc, a, b) -> np.ndarray:
+    """|dc*b| * (|t1(a)| + |t2(a)|): the magnitude the fp32 da tolerance scales by."""
+    dc, a, b = _bits(dc, dtype), _bits(a, dtype), _bits(b, dtype)
+    m = np.empty(a.shape, dtype=np.float64)
+    lib().oracle_bwd_da_scale(ACTS[act_name], DTYPES[dtype], _ptr(dc), _ptr(a), _ptr(b),
+                              _ptr(m), a.size)
+    return m
+
+
+# ---- the concatenated [gate | up] layout --------------------------------------
+
+def split_concat(x, n_cols: int):
+    """a = x[:, :I], b = x[:, I:2I] (gate half first)."""
+    x = np.asarray(x)
+    return x[:, :n_cols], x[:, n_cols:2 * n_cols]
+
+
+def fwd_concat(act_name: str, dtype: str, x, n_cols: int) -> np.ndarray:
+    a, b = split_concat(x, n_cols)
+    return fwd(act_name, dtype, a, b)
+
+
+def bwd_concat(act_name: str, dtype: str, dc, x, n_cols: int) -> np.ndarray:
+    """Gradient w.r.t. the concatenated input: dx = [da | db]."""
+    a, b = split_concat(x, n_cols)
+    da, db = bwd(act_name, dtype, dc, a, b)
+    return np.concatenate([da, db], axis=1)
+
+
+# ---- threaded drivers (the same element-wise calls, split over row blocks) -----
+
+def _row_blocks(n_rows: int, parts: int):
+    parts = max(1, min(parts, n_rows))
+    step = -(-n_rows // parts)
+    return [(r, min(n_rows, r + step)) for r in range(0, n_rows, step)]
+
+
+def fwd_threaded(act_name: str, dtype: str, a, b, threads: int) -> np.ndarray:
+    a, b = _bits(a, dtype), _bits(b, dtype)
+    y = np.empty_like(a)
+    L, code, dt = lib(), ACTS[act_name], DTYPES[dtype]
+    rows = a.reshape(a.shape[0], -1) if a.ndim > 1 else a.reshape(1, -1)
+    brow = b.reshape(rows.shape)
+    yrow = y.reshape(rows.shape)
+
+    def work(rng):
+        r0, r1 = rng
+        n = (r1 - r0) * rows.shape[1]
+        L.oracle_fwd(code, dt, _ptr(rows[r0:r1]), _ptr(brow[r0:r1]), _ptr(yrow[r0:r1]), n)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(work, _row_blocks(rows.shape[0], threads)))
+    return y
+
+
+def bwd_threaded(act_name: str, dtype: str, dc, a, b, threads: int):
+    dc, a, b = _bits(dc, dtype), _bits(a, dtype), _bits(b, dtype)
+    da, db = np.empty_like(a), np.empty_like(a)
+    L, code, dt = lib(), ACTS[act_name], DTYPES[dtype]
+    shp = (a.shape[0], -1) if a.ndim > 1 else (1, -1)
+    v = [t.reshape(shp) for t in (dc, a, b, da, db)]
+
+    def work(rng):
+        r0, r1 = rng
+        n = (r1 - r0) * v[1].shape[1]
+        L.oracle_bwd(code, dt, *[_ptr(t[r0:r1]) for t in v], n)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(work, _row_blocks(v[1].shape[0], threads)))
+    return da, db
