@@ -1,0 +1,411 @@
+"""Benchmark of the fused gated activation on GB300.
+
+One step = the whole hot path over one batch: the SwiGLU forward
+y = silu(a) * b and the backward (da, db) = (dc * silu'(a) * b, dc * silu(a))
+on bf16 matrices of 4096 x 14336 (4096 tokens at intermediate size 14336),
+through the C ABI (glu_fwd, glu_bwd).  The metric is achieved HBM bandwidth:
+algorithmic bytes (forward 3 x 2 B, backward 5 x 2 B per element) over time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs its own batch on its own GPU (weak scaling, no
+data-path collective); rank 0 prints one JSON line.  `--impl reference` times
+the double-precision CPU oracle on the host cores instead (the only other
+implementation of this computation), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import glu_synth  # noqa: E402
+
+ROWS, COLS = 4096, 14336
+E = 2
+N_ELEMS = ROWS * COLS
+FWD_BYTES = 3 * E * N_ELEMS
+BWD_BYTES = 5 * E * N_ELEMS
+STEP_BYTES = FWD_BYTES + BWD_BYTES
+METRIC = "SwiGLU fwd+bwd achieved HBM GB/s (% of GB300 peak), bf16 BT=4096 I=14336"
+UNIT = "GB/s"
+WORKLOAD = "swiglu_fwd_bwd_bf16_4096x14336"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "glu_activation_mlps_gb300", "csrc")
+
+
+def config(extra=None):
+    c = {"workload": WORKLOAD, "act": "silu", "layout": "split", "n_rows": ROWS, "n_cols": COLS,
+         "storage": "bf16", "math": "f32", "backward": "out-of-place (da, db separate)",
+         "l2": f"no flush: inputs larger than L2 ({STEP_BYTES / 1e6:.0f} MB touched per step, "
+               f"{FWD_BYTES / 1e6:.0f} MB per forward, vs {L2_BYTES / 2**20:.0f} MiB L2)",
+         "inputs": "seeded synthetic a, b, dc ~ N(0, 1)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the backward kernel from the committed ncu
+    summary, or None if the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_sha") != source_sha():
+        return None
+    return t.get("bwd_dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: str):
+        self.samples = []
+        self.proc = None
+        self.idx = device
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        deadline = time.time() + 5
+        while not self.samples and time.time() < deadline:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [s for t, s in self.samples if self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        if not rows:
+            rows = [s for _, s in self.samples][-3:]
+        try:
+            sm = [float(r[1]) for r in rows]
+            smax = max(float(r[2]) for r in rows)
+        except (ValueError, IndexError):
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows)}
+
+
+def gpu_selector(local_rank: int) -> str:
+    """nvidia-smi's id for this process's CUDA device (its UUID when known:
+    CUDA ordinals and nvidia-smi indices differ under CUDA_VISIBLE_DEVICES)."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [p for p in vis.split(",") if p.strip()]
+        return parts[local_rank].strip() if local_rank < len(parts) else str(local_rank)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import glu_activation_mlps_gb300 as glu
+    from glu_activation_mlps_gb300 import ACT, DTYPE, LAYOUT
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if local_rank == 0:
+        glu.build()
+    if world > 1:
+        torch.distributed.barrier()
+    glu.lib()
+
+    d = glu_synth.metric_bf16()
+    host = {k: torch.from_numpy(d[k].view(np.int16)).pin_memory() for k in ("a", "b", "dc")}
+    A, B, DC = (host[k].to(dev).view(torch.bfloat16) for k in ("a", "b", "dc"))
+    Y, DA, DB = (torch.empty_like(A) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    silu, split, bf16 = ACT["silu"], LAYOUT["split"], DTYPE["bf16"]
+    L = glu.lib()
+    pa, pb, pc, py, pda, pdb = (t.data_ptr() for t in (A, B, DC, Y, DA, DB))
+
+    def fwd():
+        st = L.glu_fwd(pa, COLS, pb, COLS, py, COLS, ROWS, COLS, split, silu, bf16, sh)
+        if st:
+            raise glu.GluError(st, "glu_fwd")
+
+    def bwd():
+        st = L.glu_bwd(pc, COLS, pa, COLS, pb, COLS, pda, COLS, pdb, COLS, ROWS, COLS, split, silu, bf16, sh)
+        if st:
+            raise glu.GluError(st, "glu_bwd")
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        fwd()
+        launch_fwd = dict(glu.glu_last_launch())
+        bwd()
+        launch_bwd = dict(glu.glu_last_launch())
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_selector(local_rank)) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(True)
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd()
+        ev[k][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(False)
+    barrier()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    launches = 2 * K
+    clock_info = clocks.stop() if clocks else None
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the same C ABI with host buffers: copy a, b, dc in
+    # from pinned host memory, run both kernels, copy y, da, db back out
+    out_host = {k: torch.empty_like(host["a"]).pin_memory() for k in ("y", "da", "db")}
+    Ke = max(3, min(K, 20))
+
+    def e2e_step():
+        A.view(torch.int16).copy_(host["a"], non_blocking=True)
+        B.view(torch.int16).copy_(host["b"], non_blocking=True)
+        DC.view(torch.int16).copy_(host["dc"], non_blocking=True)
+        fwd()
+        bwd()
+        out_host["y"].copy_(Y.view(torch.int16), non_blocking=True)
+        out_host["da"].copy_(DA.view(torch.int16), non_blocking=True)
+        out_host["db"].copy_(DB.view(torch.int16), non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    barrier()
+
+    if rank != 0:
+        return None
+
+    peak, peak_src = measured_peak()
+    bwd_avg = statistics.fmean(bwd_ms)
+    fwd_avg = statistics.fmean(fwd_ms)
+    achieved = BWD_BYTES / (bwd_avg * 1e-3) / 1e9
+    traffic = ncu_traffic()
+    value = world * K * STEP_BYTES / (total_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config({"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                          "launch": {"fwd": launch_fwd, "bwd": launch_bwd}}),
+        "roofline": {"bound": "hbm", "kernel": "backward (glu_bwd)", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": BWD_BYTES},
+        "per_kernel": {"fwd_ms": round(fwd_avg, 5), "bwd_ms": round(bwd_avg, 5),
+                       "fwd_gbs": round(FWD_BYTES / (fwd_avg * 1e-3) / 1e9, 1),
+                       "bwd_gbs": round(achieved, 1),
+                       "fwd_frac": round(FWD_BYTES / (fwd_avg * 1e-3) / 1e9 / peak, 4),
+                       "fwd_min_ms": round(min(fwd_ms), 5), "bwd_min_ms": round(min(bwd_ms), 5)},
+        "e2e": {"value": round(world * Ke * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                "h2d_bytes_per_step": 3 * E * N_ELEMS, "d2h_bytes_per_step": 3 * E * N_ELEMS,
+                "steps": Ke, "ms_per_step": round(e2e_ms / Ke, 4)},
+        "gpu_launches": launches,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, budget_s=args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle arms
+
+def oracle_rows(orc, d, r0, r1, threads):
+    a, b, dc = d["a"][r0:r1], d["b"][r0:r1], d["dc"][r0:r1]
+    orc.fwd_threaded("silu", "bf16", a, b, threads)
+    orc.bwd_threaded("silu", "bf16", dc, a, b, threads)
+
+
+def cpu_baseline(d, budget_s=3.0):
+    """The oracle, as it stands, on the host cores: consecutive 128-row blocks
+    of the workload until `budget_s` of wall time has passed (or all rows)."""
+    import oracle as orc
+    orc.build()
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    rows = 0
+    while rows < ROWS and (time.perf_counter() - t0) < budget_s:
+        r1 = min(ROWS, rows + 128)
+        oracle_rows(orc, d, rows, r1, threads)
+        rows = r1
+    dt = time.perf_counter() - t0
+    nbytes = rows * COLS * 8 * E
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows} of the 4096x14336 bf16 workload (fwd + bwd, "
+                      f"{rows * COLS} elements, {dt:.2f} s wall on {threads} threads)"}
+
+
+def run_reference(args):
+    """The double-precision CPU oracle timed as the reference arm: every step
+    runs forward + backward on a block of rows of the same workload."""
+    import oracle as orc
+    orc.build()
+    d = glu_synth.metric_bf16()
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle_rows(orc, d, 0, 16, threads)
+    per_row = (time.perf_counter() - t0) / 16
+    total_steps = args.steps + args.warmup
+    rows = int(max(1, min(ROWS, args.ref_seconds / max(total_steps, 1) / max(per_row, 1e-9))))
+    for k in range(args.warmup):
+        oracle_rows(orc, d, 0, rows, threads)
+    times = []
+    for k in range(args.steps):
+        s = time.perf_counter()
+        oracle_rows(orc, d, 0, rows, threads)
+        times.append(time.perf_counter() - s)
+    total = sum(times)
+    nbytes = rows * COLS * 8 * E
+    value = args.steps * nbytes / total / 1e9
+    sample = f"rows 0..{rows} of the 4096x14336 bf16 workload per step (fwd + bwd, {rows * COLS} elements)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config({"parallelism": f"{threads} host threads", "math": "f64"}),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=3.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

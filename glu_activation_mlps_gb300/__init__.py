@@ -1,0 +1,255 @@
+"""Python binding of the fused gated-activation library (GB300, sm_103a).
+
+``libglu_gb300.so`` exports the C ABI declared in ``include/glu.h``.  This
+module only marshals arguments: every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback; if the library has not been
+built, every call raises.
+
+Two levels:
+  * ``glu_fwd`` / ``glu_bwd`` / ``glu_status_string`` / ... : the C entry points
+    with the same names and arguments (raw device addresses as ints, strides
+    in elements, enum codes, the stream handle as an int);
+  * ``fwd`` / ``bwd``: the same calls taking torch CUDA tensors, reading
+    pointers and strides from the tensors' metadata.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libglu_gb300.so")
+
+ACT = {"silu": 0, "gelu_erf": 1, "gelu_tanh": 2, "relu": 3}
+LAYOUT = {"split": 0, "concat": 1}
+DTYPE = {"f32": 0, "f16": 1, "bf16": 2}
+STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STRIDE",
+          -4: "GLU_ERR_ALIAS", -5: "GLU_ERR_ENUM", -6: "GLU_ERR_CUDA"}
+
+# Every symbol include/glu.h declares.
+EXPORTS = ("glu_fwd", "glu_bwd", "glu_status_string", "glu_last_cuda_error", "glu_version",
+           "glu_last_launch", "glu_set_tuning", "glu_get_tuning")
+
+
+class GluError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)} ({glu_status_string(status)})"
+        if status == -6:
+            msg += ": " + glu_last_cuda_error()
+        super().__init__(msg)
+
+
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [("launched", ctypes.c_int32), ("backward", ctypes.c_int32),
+                ("vec_bytes", ctypes.c_int32), ("unroll", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("flattened", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("vector_units", ctypes.c_int64), ("tail_elems", ctypes.c_int64)]
+
+
+class Tuning(ctypes.Structure):
+    _fields_ = [("vec_bytes", ctypes.c_int32), ("unroll", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(glu_activation_mlps_gb300.build()); there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+            L.glu_fwd.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci, vp]
+            L.glu_fwd.restype = ci
+            L.glu_bwd.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci, vp]
+            L.glu_bwd.restype = ci
+            L.glu_status_string.argtypes = [ci]
+            L.glu_status_string.restype = ctypes.c_char_p
+            L.glu_last_cuda_error.argtypes = []
+            L.glu_last_cuda_error.restype = ctypes.c_char_p
+            L.glu_version.argtypes = []
+            L.glu_version.restype = ci
+            L.glu_last_launch.argtypes = [ctypes.POINTER(LaunchInfo)]
+            L.glu_last_launch.restype = ci
+            L.glu_set_tuning.argtypes = [ctypes.POINTER(Tuning)]
+            L.glu_set_tuning.restype = ci
+            L.glu_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
+            L.glu_get_tuning.restype = ci
+            _lib = L
+    return _lib
+
+
+# ---- the C entry points -------------------------------------------------------
+
+def glu_fwd(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols, layout, act, dtype, stream) -> int:
+    return lib().glu_fwd(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols,
+                         layout, act, dtype, stream)
+
+
+def glu_bwd(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_stride,
+            n_rows, n_cols, layout, act, dtype, stream) -> int:
+    return lib().glu_bwd(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_stride,
+                         n_rows, n_cols, layout, act, dtype, stream)
+
+
+def glu_status_string(status: int) -> str:
+    return lib().glu_status_string(status).decode()
+
+
+def glu_last_cuda_error() -> str:
+    return lib().glu_last_cuda_error().decode()
+
+
+def glu_version() -> int:
+    return lib().glu_version()
+
+
+def glu_last_launch() -> dict:
+    info = LaunchInfo()
+    st = lib().glu_last_launch(ctypes.byref(info))
+    if st:
+        raise GluError(st, "glu_last_launch")
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_ if f != "reserved"}
+
+
+def glu_set_tuning(vec_bytes: int = 0, unroll: int = 0, ctas_per_sm: int = 0) -> None:
+    t = Tuning(vec_bytes, unroll, ctas_per_sm, 0)
+    st = lib().glu_set_tuning(ctypes.byref(t))
+    if st:
+        raise GluError(st, "glu_set_tuning")
+
+
+def glu_get_tuning() -> dict:
+    t = Tuning()
+    st = lib().glu_get_tuning(ctypes.byref(t))
+    if st:
+        raise GluError(st, "glu_get_tuning")
+    return {"vec_bytes": t.vec_bytes, "unroll": t.unroll, "ctas_per_sm": t.ctas_per_sm}
+
+
+# ---- torch tensor marshalling -------------------------------------------------
+
+def _dtype_code(t) -> int:
+    import torch
+    m = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float32, float16 or bfloat16")
+    return m[t.dtype]
+
+
+def _rows(t, name):
+    """(n_rows, row stride) of a tensor viewed as a matrix over its last dim."""
+    if t.dim() < 1 or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor with at least one dimension")
+    if t.stride(-1) != 1 and t.shape[-1] > 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    if t.dim() == 1:
+        return 1, t.shape[0]
+    lead = t.shape[:-1]
+    # leading dims must collapse to one row index with a single stride
+    stride = t.stride(-2)
+    expect = stride
+    for d in range(t.dim() - 2, -1, -1):
+        if t.shape[d] != 1 and t.stride(d) != expect:
+            raise ValueError(f"{name}: leading dimensions do not collapse to one row stride")
+        expect *= t.shape[d]
+    n = 1
+    for s in lead:
+        n *= s
+    return n, stride
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fwd(a, b=None, *, y=None, act: str = "silu", layout: str = "split", stream=None):
+    """y = act(a) * b on CUDA tensors.  SPLIT: a, b of one shape (..., I).
+    CONCAT: a is x of shape (..., 2I), b is None.  ``y`` may be given (also as
+    b, or as x[..., I:], for in-place); otherwise it is allocated."""
+    import torch
+    if layout not in LAYOUT:
+        raise ValueError(layout)
+    concat = layout == "concat"
+    n_rows, a_stride = _rows(a, "a")
+    if concat:
+        if a.shape[-1] % 2:
+            raise ValueError("concat input needs an even last dimension")
+        n_cols = a.shape[-1] // 2
+        b_ptr, b_stride = None, 0
+        out_shape = (*a.shape[:-1], n_cols)
+    else:
+        if b is None or b.shape != a.shape or b.dtype != a.dtype:
+            raise ValueError("b must match a in shape and dtype")
+        n_cols = a.shape[-1]
+        _, b_stride = _rows(b, "b")
+        b_ptr = b.data_ptr()
+        out_shape = a.shape
+    if y is None:
+        y = torch.empty(out_shape, dtype=a.dtype, device=a.device)
+    if tuple(y.shape) != tuple(out_shape) or y.dtype != a.dtype:
+        raise ValueError("y has the wrong shape or dtype")
+    _, y_stride = _rows(y, "y")
+    st = glu_fwd(a.data_ptr(), a_stride, b_ptr, b_stride, y.data_ptr(), y_stride,
+                 n_rows, n_cols, LAYOUT[layout], ACT[act], _dtype_code(a), _stream(stream))
+    if st:
+        raise GluError(st, "glu_fwd")
+    return y
+
+
+def bwd(dc, a, b=None, *, da=None, db=None, act: str = "silu", layout: str = "split",
+        inplace: bool = False, stream=None):
+    """(da, db) = (dc * act'(a) * b, dc * act(a)).  SPLIT returns (da, db);
+    CONCAT (a = x, b None) returns dx = [da | db].  ``inplace`` writes da over
+    a and db over b (dx over x)."""
+    import torch
+    concat = layout == "concat"
+    n_rows, a_stride = _rows(a, "a")
+    _, dc_stride = _rows(dc, "dc")
+    code = _dtype_code(a)
+    if concat:
+        n_cols = a.shape[-1] // 2
+        if dc.shape[-1] != n_cols:
+            raise ValueError("dc must have half the width of x")
+        dx = a if inplace else (da if da is not None else torch.empty_like(a))
+        _, dx_stride = _rows(dx, "dx")
+        st = glu_bwd(dc.data_ptr(), dc_stride, a.data_ptr(), a_stride, None, 0,
+                     dx.data_ptr(), dx_stride, None, 0, n_rows, n_cols,
+                     LAYOUT[layout], ACT[act], code, _stream(stream))
+        if st:
+            raise GluError(st, "glu_bwd")
+        return dx
+    if b is None or b.shape != a.shape or dc.shape != a.shape:
+        raise ValueError("dc, a and b must have one shape")
+    n_cols = a.shape[-1]
+    _, b_stride = _rows(b, "b")
+    if inplace:
+        da, db = a, b
+    da = da if da is not None else torch.empty_like(a)
+    db = db if db is not None else torch.empty_like(b)
+    _, da_stride = _rows(da, "da")
+    _, db_stride = _rows(db, "db")
+    st = glu_bwd(dc.data_ptr(), dc_stride, a.data_ptr(), a_stride, b.data_ptr(), b_stride,
+                 da.data_ptr(), da_stride, db.data_ptr(), db_stride, n_rows, n_cols,
+                 LAYOUT[layout], ACT[act], code, _stream(stream))
+    if st:
+        raise GluError(st, "glu_bwd")
+    return da, db

@@ -1,0 +1,378 @@
+// C-ABI front end: argument validation, aliasing rules, launch planning and
+// dispatch to the per-dtype kernel tables.  Declarations and the contract of
+// every entry point are in include/glu.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "glu.h"
+#include "glu_plan.h"
+
+namespace {
+
+using glu::Params;
+
+thread_local glu_launch_info_t t_last_launch{};
+thread_local char t_cuda_error[256] = "";
+
+// Process-wide tuning; 0 = library default.  Defaults: 32-byte accesses where
+// the operands allow it, two accesses per operand in flight per thread, and a
+// grid of one block per tile (no persistent reuse).
+std::atomic<int32_t> g_vec_bytes{0};
+std::atomic<int32_t> g_unroll{0};
+std::atomic<int32_t> g_ctas_per_sm{0};
+constexpr int32_t kDefaultVecBytes = 32;
+constexpr int32_t kDefaultUnroll = 2;
+constexpr int32_t kDefaultCtasPerSm = -1;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int elem_size(int dtype) { return dtype == GLU_F32 ? 4 : 2; }
+
+bool valid_enums(int layout, int act, int dtype)
+{
+    return (layout == GLU_LAYOUT_SPLIT || layout == GLU_LAYOUT_CONCAT) &&
+           (act >= GLU_ACT_SILU && act <= GLU_ACT_RELU) &&
+           (dtype == GLU_F32 || dtype == GLU_F16 || dtype == GLU_BF16);
+}
+
+// A matrix operand: base address, row stride and row width in elements.
+struct Mat {
+    uintptr_t p;
+    int64_t stride;
+    int64_t width;
+};
+
+// Byte extent of a matrix: ((rows - 1) * stride + width) * E, or -1 on overflow.
+int64_t extent_bytes(const Mat &m, int64_t rows, int E)
+{
+    int64_t last, span, bytes;
+    if (__builtin_mul_overflow(rows - 1, m.stride, &last)) return -1;
+    if (__builtin_add_overflow(last, m.width, &span)) return -1;
+    if (__builtin_mul_overflow(span, int64_t(E), &bytes)) return -1;
+    if (uint64_t(bytes) > UINTPTR_MAX - m.p) return -1;
+    return bytes;
+}
+
+// Do the element sets of X and Y (same rows, same width C, element size E)
+// share an address?  Exact for equal strides; conservative (overlapping
+// footprints count as overlap) otherwise.
+bool elems_overlap(const Mat &X, const Mat &Y, int64_t rows, int E)
+{
+    const uint64_t x0 = X.p, x1 = X.p + uint64_t(extent_bytes(X, rows, E));
+    const uint64_t y0 = Y.p, y1 = Y.p + uint64_t(extent_bytes(Y, rows, E));
+    if (x1 <= y0 || y1 <= x0) return false;
+    if (rows == 1 || X.stride != Y.stride) return true;
+    const int64_t diff = int64_t(Y.p - X.p);
+    if (diff % E != 0) return true;
+    // Y's (r, c) is X's element d + r*s + c.  A shared element needs a row
+    // offset k with |k| < rows and |d - k s| < C; since C <= s only
+    // k = floor(d / s) and k + 1 can qualify.
+    const int64_t d = diff / E, s = X.stride, C = X.width;
+    int64_t k = d / s;
+    if ((d % s != 0) && ((d < 0) != (s < 0))) --k;          // floor division
+    for (int64_t kk = k; kk <= k + 1; ++kk) {
+        const int64_t r = d - kk * s;
+        if ((kk < rows && -kk < rows) && (r < C && -r < C)) return true;
+    }
+    return false;
+}
+
+bool same_mat(const Mat &X, const Mat &Y, int64_t rows)
+{
+    return X.p == Y.p && (rows == 1 || X.stride == Y.stride) && X.width == Y.width;
+}
+
+// Outputs may equal an input exactly; any other overlap is an error, and two
+// outputs may not overlap at all.
+int check_aliasing(const Mat *in, int n_in, const Mat *out, int n_out, int64_t rows, int E)
+{
+    for (int o = 0; o < n_out; ++o) {
+        for (int i = 0; i < n_in; ++i)
+            if (!same_mat(out[o], in[i], rows) && elems_overlap(out[o], in[i], rows, E))
+                return GLU_ERR_ALIAS;
+        for (int q = o + 1; q < n_out; ++q)
+            if (elems_overlap(out[o], out[q], rows, E)) return GLU_ERR_ALIAS;
+    }
+    return GLU_OK;
+}
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+    if (dev < kMaxDevices) {
+        int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev < kMaxDevices) g_sm_count[dev].store(c, std::memory_order_relaxed);
+    return c;
+}
+
+int cuda_fail(cudaError_t e)
+{
+    snprintf(t_cuda_error, sizeof(t_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return GLU_ERR_CUDA;
+}
+
+// Everything the planner needs about one call after validation.  Strides are
+// in elements; ptrs/strides list every operand (inputs then outputs).
+struct Call {
+    int dir, act, dtype, E;
+    int64_t rows, cols;
+    const char *a, *b, *dc;
+    char *y0, *y1;
+    int64_t sa, sb, sdc, sy0, sy1;
+};
+
+int plan_and_launch(const Call &c, cudaStream_t stream)
+{
+    const int E = c.E;
+    const int n_ops = c.dir == glu::kBwd ? 5 : 3;
+    const uintptr_t ptrs[5] = {uintptr_t(c.a), uintptr_t(c.b), uintptr_t(c.y0),
+                               uintptr_t(c.dc), uintptr_t(c.y1)};
+    const int64_t strides[5] = {c.sa, c.sb, c.sy0, c.sdc, c.sy1};
+
+    // Rows that are contiguous in every operand are one long row.
+    bool flat = c.rows == 1;
+    if (!flat) {
+        flat = true;
+        for (int i = 0; i < n_ops; ++i) flat = flat && strides[i] == c.cols;
+    }
+    const int64_t R = flat ? 1 : c.rows;
+    const int64_t C = flat ? c.rows * c.cols : c.cols;   // fits: extents were checked
+
+    // Widest access every operand's rows are aligned to.
+    int32_t cap = g_vec_bytes.load(std::memory_order_relaxed);
+    if (cap == 0) cap = kDefaultVecBytes;
+    int vb = 0;
+    for (int cand : {32, 16}) {
+        if (cand > cap) continue;
+        bool ok = true;
+        for (int i = 0; i < n_ops; ++i) {
+            ok = ok && (ptrs[i] % cand == 0);
+            if (!flat) ok = ok && ((strides[i] * E) % cand == 0);
+        }
+        if (ok) { vb = cand; break; }
+    }
+    int32_t unroll = g_unroll.load(std::memory_order_relaxed);
+    if (unroll == 0) unroll = kDefaultUnroll;
+    const int unroll_sel = unroll == 1 ? 0 : (unroll == 2 ? 1 : 2);
+    const int vb_sel = vb == 32 ? 0 : (vb == 16 ? 1 : 2);
+    if (vb == 0) unroll = 1;
+
+    Params p{};
+    p.a = c.a; p.b = c.b; p.dc = c.dc; p.y0 = c.y0; p.y1 = c.y1;
+    p.sa = c.sa * E; p.sb = c.sb * E; p.sdc = c.sdc * E; p.sy0 = c.sy0 * E; p.sy1 = c.sy1 * E;
+    p.rows = R;
+    const int64_t per_unit = vb ? vb / E : 0;
+    p.vpr = per_unit ? C / per_unit : 0;
+    p.units = R * p.vpr;
+    p.rem = C - p.vpr * per_unit;
+    p.tail_units = R * p.rem;
+    p.tail_col_bytes = p.vpr * vb;
+    p.wide = p.units >= (int64_t(1) << 32);
+    if (p.units > 0 && R > 1 && !p.wide) glu::fastdiv_init(uint32_t(p.vpr), &p.div_magic, &p.div_shift);
+    p.tail_wide = p.tail_units >= (int64_t(1) << 32);
+    if (p.tail_units > 0 && R > 1 && !p.tail_wide) glu::fastdiv_init(uint32_t(p.rem), &p.tail_magic, &p.tail_shift);
+
+    glu::KernelFn fn = nullptr;
+    switch (c.dtype) {
+    case GLU_F32: fn = glu::kernel_f32(c.act, c.dir, vb_sel, unroll_sel); break;
+    case GLU_F16: fn = glu::kernel_f16(c.act, c.dir, vb_sel, unroll_sel); break;
+    default: fn = glu::kernel_bf16(c.act, c.dir, vb_sel, unroll_sel); break;
+    }
+    if (!fn) return GLU_ERR_ENUM;
+
+    // Grid: one block per tile of kThreads * unroll units (and enough blocks
+    // for the scalar tail), or a persistent grid of ctas_per_sm blocks per SM.
+    const int64_t tile = int64_t(glu::kThreads) * unroll;
+    int64_t blocks = (p.units + tile - 1) / tile;
+    const int64_t tail_blocks = (p.tail_units + glu::kThreads - 1) / glu::kThreads;
+    if (tail_blocks > blocks) blocks = tail_blocks;
+    if (blocks < 1) blocks = 1;
+    int32_t per_sm = g_ctas_per_sm.load(std::memory_order_relaxed);
+    if (per_sm == 0) per_sm = kDefaultCtasPerSm;
+    if (per_sm > 0) {
+        const int sms = sm_count();
+        if (sms <= 0) return cuda_fail(cudaGetLastError());
+        if (blocks > int64_t(per_sm) * sms) blocks = int64_t(per_sm) * sms;
+    }
+    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+
+    void *args[] = {&p};
+    cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(blocks)),
+                                     dim3(glu::kThreads), args, 0, stream);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cuda_fail(e);
+    }
+
+    glu_launch_info_t info{};
+    info.launched = 1;
+    info.backward = c.dir == glu::kBwd;
+    info.vec_bytes = vb ? vb : E;
+    info.unroll = unroll;
+    info.threads = glu::kThreads;
+    info.grid = int32_t(blocks);
+    info.flattened = flat && c.rows > 1;
+    info.vector_units = p.units;
+    info.tail_elems = p.tail_units;
+    t_last_launch = info;
+    return GLU_OK;
+}
+
+void mark_noop()
+{
+    t_last_launch = glu_launch_info_t{};
+}
+
+}  // namespace
+
+extern "C" {
+
+int glu_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, void *y,
+            int64_t y_stride, int64_t n_rows, int64_t n_cols, glu_layout_t layout,
+            glu_act_t act, glu_dtype_t dtype, glu_stream_t stream)
+{
+    if (!valid_enums(layout, act, dtype)) return GLU_ERR_ENUM;
+    if (n_rows < 0 || n_cols < 0) return GLU_ERR_SHAPE;
+    if (n_rows == 0 || n_cols == 0) { mark_noop(); return GLU_OK; }
+    const bool concat = layout == GLU_LAYOUT_CONCAT;
+    if (!a || !y || (!concat && !b)) return GLU_ERR_NULL;
+    const int E = elem_size(dtype);
+    if (n_rows == 1) { a_stride = concat ? 2 * n_cols : n_cols; b_stride = n_cols; y_stride = n_cols; }
+    if (concat) {
+        if (n_cols > INT64_MAX / 2) return GLU_ERR_SHAPE;
+        if (a_stride < 2 * n_cols) return GLU_ERR_STRIDE;
+        b = static_cast<const char *>(a) + n_cols * E;
+        b_stride = a_stride;
+    } else if (a_stride < n_cols || b_stride < n_cols) {
+        return GLU_ERR_STRIDE;
+    }
+    if (y_stride < n_cols) return GLU_ERR_STRIDE;
+
+    const Mat ma{uintptr_t(a), a_stride, n_cols}, mb{uintptr_t(b), b_stride, n_cols};
+    const Mat my{uintptr_t(y), y_stride, n_cols};
+    const Mat mx{uintptr_t(a), a_stride, concat ? 2 * n_cols : n_cols};
+    if (extent_bytes(mx, n_rows, E) < 0 || extent_bytes(mb, n_rows, E) < 0 ||
+        extent_bytes(my, n_rows, E) < 0)
+        return GLU_ERR_SHAPE;
+    const Mat ins[2] = {ma, mb};
+    if (int s = check_aliasing(ins, 2, &my, 1, n_rows, E)) return s;
+
+    Call c{};
+    c.dir = glu::kFwd; c.act = act; c.dtype = dtype; c.E = E;
+    c.rows = n_rows; c.cols = n_cols;
+    c.a = static_cast<const char *>(a); c.b = static_cast<const char *>(b);
+    c.y0 = static_cast<char *>(y);
+    c.sa = a_stride; c.sb = b_stride; c.sy0 = y_stride;
+    return plan_and_launch(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int glu_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
+            int64_t b_stride, void *da, int64_t da_stride, void *db, int64_t db_stride,
+            int64_t n_rows, int64_t n_cols, glu_layout_t layout, glu_act_t act,
+            glu_dtype_t dtype, glu_stream_t stream)
+{
+    if (!valid_enums(layout, act, dtype)) return GLU_ERR_ENUM;
+    if (n_rows < 0 || n_cols < 0) return GLU_ERR_SHAPE;
+    if (n_rows == 0 || n_cols == 0) { mark_noop(); return GLU_OK; }
+    const bool concat = layout == GLU_LAYOUT_CONCAT;
+    if (!dc || !a || !da || (!concat && (!b || !db))) return GLU_ERR_NULL;
+    const int E = elem_size(dtype);
+    if (n_rows == 1) {
+        dc_stride = n_cols;
+        a_stride = da_stride = concat ? 2 * n_cols : n_cols;
+        b_stride = db_stride = n_cols;
+    }
+    if (concat) {
+        if (n_cols > INT64_MAX / 2) return GLU_ERR_SHAPE;
+        if (a_stride < 2 * n_cols || da_stride < 2 * n_cols) return GLU_ERR_STRIDE;
+        b = static_cast<const char *>(a) + n_cols * E;
+        b_stride = a_stride;
+        db = static_cast<char *>(da) + n_cols * E;
+        db_stride = da_stride;
+    } else if (a_stride < n_cols || b_stride < n_cols || da_stride < n_cols || db_stride < n_cols) {
+        return GLU_ERR_STRIDE;
+    }
+    if (dc_stride < n_cols) return GLU_ERR_STRIDE;
+
+    const Mat mc{uintptr_t(dc), dc_stride, n_cols};
+    const Mat ma{uintptr_t(a), a_stride, n_cols}, mb{uintptr_t(b), b_stride, n_cols};
+    const Mat mda{uintptr_t(da), da_stride, n_cols}, mdb{uintptr_t(db), db_stride, n_cols};
+    const Mat mx{uintptr_t(a), a_stride, concat ? 2 * n_cols : n_cols};
+    const Mat mdx{uintptr_t(da), da_stride, concat ? 2 * n_cols : n_cols};
+    if (extent_bytes(mc, n_rows, E) < 0 || extent_bytes(mx, n_rows, E) < 0 ||
+        extent_bytes(mb, n_rows, E) < 0 || extent_bytes(mdx, n_rows, E) < 0 ||
+        extent_bytes(mdb, n_rows, E) < 0)
+        return GLU_ERR_SHAPE;
+    const Mat ins[3] = {mc, ma, mb};
+    const Mat outs[2] = {mda, mdb};
+    if (int s = check_aliasing(ins, 3, outs, 2, n_rows, E)) return s;
+
+    Call c{};
+    c.dir = glu::kBwd; c.act = act; c.dtype = dtype; c.E = E;
+    c.rows = n_rows; c.cols = n_cols;
+    c.a = static_cast<const char *>(a); c.b = static_cast<const char *>(b);
+    c.dc = static_cast<const char *>(dc);
+    c.y0 = static_cast<char *>(da); c.y1 = static_cast<char *>(db);
+    c.sa = a_stride; c.sb = b_stride; c.sdc = dc_stride; c.sy0 = da_stride; c.sy1 = db_stride;
+    return plan_and_launch(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *glu_status_string(int status)
+{
+    switch (status) {
+    case GLU_OK: return "ok";
+    case GLU_ERR_NULL: return "a required pointer is NULL";
+    case GLU_ERR_SHAPE: return "negative size, or a size whose byte extent overflows";
+    case GLU_ERR_STRIDE: return "a row stride is smaller than its row width";
+    case GLU_ERR_ALIAS: return "an output overlaps an input other than exactly, or another output";
+    case GLU_ERR_ENUM: return "unknown activation, layout, dtype or tuning value";
+    case GLU_ERR_CUDA: return "the CUDA runtime refused the launch";
+    default: return "unknown status";
+    }
+}
+
+const char *glu_last_cuda_error(void) { return t_cuda_error; }
+
+int glu_version(void) { return GLU_VERSION; }
+
+int glu_last_launch(glu_launch_info_t *out)
+{
+    if (!out) return GLU_ERR_NULL;
+    *out = t_last_launch;
+    return GLU_OK;
+}
+
+int glu_set_tuning(const glu_tuning_t *t)
+{
+    if (!t) return GLU_ERR_NULL;
+    const int32_t v = t->vec_bytes, u = t->unroll, c = t->ctas_per_sm;
+    if (!(v == 0 || v == 32 || v == 16 || v == 4 || v == 2)) return GLU_ERR_ENUM;
+    if (!(u == 0 || u == 1 || u == 2 || u == 4)) return GLU_ERR_ENUM;
+    if (c > 64) return GLU_ERR_ENUM;
+    g_vec_bytes.store(v);
+    g_unroll.store(u);
+    g_ctas_per_sm.store(c);
+    return GLU_OK;
+}
+
+int glu_get_tuning(glu_tuning_t *out)
+{
+    if (!out) return GLU_ERR_NULL;
+    out->vec_bytes = g_vec_bytes.load();
+    out->unroll = g_unroll.load();
+    out->ctas_per_sm = g_ctas_per_sm.load();
+    out->reserved = 0;
+    return GLU_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,11 @@
+// Kernel instantiations for storage dtype f32 (all activations, both directions).
+#include "glu_kernels.cuh"
+
+namespace glu {
+
+KernelFn kernel_f32(int act, int dir, int vb_sel, int unroll_sel)
+{
+    return select_kernel<float>(act, dir, vb_sel, unroll_sel);
+}
+
+}  // namespace glu

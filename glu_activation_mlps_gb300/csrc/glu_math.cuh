@@ -1,0 +1,187 @@
+// fp32 device math of the four gated activations, forward and backward.
+//
+// Formulas: "Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel" (Required
+// reasoning process steps 5 and 7; Common failure modes, "GELU variant
+// mismatch") and "Kernel Profile: SwiGLU (Tier 1 - Element-wise)" (Backward
+// Pass).  Everything is evaluated in fp32 ("Kernel design rules": sigmoid and
+// GELU in fp32 for fp16/bf16 inputs), without flush-to-zero.
+//
+// Rewrites used for accuracy (each an exact identity):
+//   sigmoid(x)          = 1/(1+e) for x >= 0, e/(1+e) for x < 0, e = exp(-|x|)
+//                         (exp never overflows; "Kernel design rules" ask for a
+//                         form that is stable for very negative x)
+//   silu'(x)            = sigmoid + x*sigmoid*(1 - sigmoid)
+//                       = (1 + e + x e) / (1+e)^2            for x >= 0
+//                       = e (1 + x + e) / (1+e)^2            for x < 0
+//                         (the only cancellation left is (1 + x) + e near the
+//                         root x* = -1.2785, where 1 + x is exact in fp32)
+//   1 + erf(z)          = erfc(-z)              (no cancellation for z < 0)
+//   0.5 (1 + tanh(u))   = sigmoid(2u)           (no cancellation for u < 0)
+//
+// `Exact` selects the variant used when the storage dtype is fp32: there the
+// rounding of the scaled arguments (x/sqrt2, the tanh polynomial, x^2) would be
+// amplified by up to 2z^2 in the tails, so those arguments are carried as
+// (hi, lo) float pairs and the first-order effect of `lo` is applied
+// analytically.  For fp16/bf16 outputs the plain fp32 forms are far below
+// half an output ulp and the corrections are skipped.
+#pragma once
+#include <cuda_runtime.h>
+#include <math.h>
+
+namespace glu {
+
+struct SigmoidParts {
+    float e;      // exp(-|x|), in (0, 1]
+    float r;      // 1 / (1 + e), in [0.5, 1)
+    float s;      // sigmoid(x)
+    float sm;     // 1 - sigmoid(x) = sigmoid(-x), formed without cancellation
+};
+
+__device__ __forceinline__ SigmoidParts sigmoid_parts(float x)
+{
+    SigmoidParts p;
+    p.e = expf(-fabsf(x));
+    p.r = __frcp_rn(1.0f + p.e);
+    float er = __fmul_rn(p.e, p.r);
+    p.s = x >= 0.0f ? p.r : er;
+    p.sm = x >= 0.0f ? er : p.r;
+    return p;
+}
+
+// (hi, lo) splits of constants: hi is the nearest float, lo the nearest float
+// to the remainder.
+constexpr float kInvSqrt2Hi = 0.707106769f;         // 1/sqrt(2)
+constexpr float kInvSqrt2Lo = 1.21016175e-08f;
+constexpr float kTwoOverSqrtPi = 1.12837923f;       // 2/sqrt(pi) = -d/dz erfc(z) at 0
+constexpr float kInvSqrt2Pi = 0.398942292f;         // 1/sqrt(2 pi)
+// tanh form: w(x) = 2u(x) = C1 x + C3 x^3 with C1 = 2 sqrt(2/pi), C3 = C1 * 0.044715
+constexpr float kC1Hi = 1.59576917f;
+constexpr float kC1Lo = -4.53406805e-08f;
+constexpr float kC3Hi = 0.0713548139f;
+constexpr float kC3Lo = 2.39883247e-09f;
+
+// erfc(-x / sqrt 2), the 2 Phi(x) of the GeGLU erf form.
+template <bool Exact>
+__device__ __forceinline__ float two_phi(float x)
+{
+    float zh = __fmul_rn(-x, kInvSqrt2Hi);
+    float v = erfcf(zh);
+    if (Exact) {
+        // z = zh + zl exactly up to the lo constant; erfc(zh + zl) =
+        // erfc(zh) - (2/sqrt pi) exp(-zh^2) zl to first order.
+        float zl = fmaf(-x, kInvSqrt2Hi, -zh) + (-x) * kInvSqrt2Lo;
+        float g = expf(-zh * zh);            // 0 (not NaN) once zh^2 overflows
+        v = fmaf(-kTwoOverSqrtPi * g, zl, v);
+    }
+    return v;
+}
+
+// w(x) = 2 sqrt(2/pi) (x + 0.044715 x^3) as hi (+ lo when Exact).
+template <bool Exact>
+__device__ __forceinline__ float tanh_arg(float x, float *lo)
+{
+    float p = __fmul_rn(x, x);
+    float inner = fmaf(kC3Hi, p, kC1Hi);     // C1 + C3 x^2
+    float w = __fmul_rn(x, inner);
+    *lo = 0.0f;
+    if (Exact && fabsf(x) < 1.0e4f) {        // beyond, sigmoid(w) is exactly 0 or 1
+        float pe = fmaf(x, x, -p);                         // x^2 = p + pe exactly
+        float q = __fmul_rn(kC3Hi, p);
+        float qe = fmaf(kC3Hi, p, -q);                     // C3hi p = q + qe exactly
+        float s = __fadd_rn(kC1Hi, q);                     // two-sum of C1hi + q
+        float bb = __fsub_rn(s, kC1Hi);
+        float se = __fadd_rn(__fsub_rn(kC1Hi, __fsub_rn(s, bb)), __fsub_rn(q, bb));
+        float slo = se + qe + kC3Hi * pe + kC3Lo * p + kC1Lo;
+        float wh = __fmul_rn(x, s);
+        float we = fmaf(x, s, -wh) + x * slo;
+        w = wh;
+        *lo = we;
+    }
+    return w;
+}
+
+// --------------------------------------------------------------------------
+// Each activation: act(x) for the forward, and (act, act') for the backward.
+
+struct Silu {
+    template <bool Exact>
+    __device__ __forceinline__ static float fwd(float x)
+    {
+        SigmoidParts p = sigmoid_parts(x);
+        return x * p.s;
+    }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        SigmoidParts p = sigmoid_parts(x);
+        *act = x * p.s;
+        float num = x >= 0.0f ? fmaf(x, p.e, 1.0f + p.e)      // 1 + e + x e
+                              : p.e * ((1.0f + x) + p.e);     // e (1 + x + e)
+        *dact = num * (p.r * p.r);
+    }
+};
+
+struct GeluErf {
+    template <bool Exact>
+    __device__ __forceinline__ static float fwd(float x)
+    {
+        return 0.5f * x * two_phi<Exact>(x);
+    }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        float phi2 = two_phi<Exact>(x);                     // 2 Phi(x)
+        float ax = fminf(fabsf(x), 40.0f);                  // phi(40) is 0 in fp32
+        float p = __fmul_rn(ax, ax);
+        float g = expf(-0.5f * p);
+        if (Exact) g = g * (1.0f - 0.5f * fmaf(ax, ax, -p));  // x^2 = p + pe
+        float pdf = kInvSqrt2Pi * g;                        // phi(x)
+        *act = 0.5f * x * phi2;
+        *dact = fmaf(x, pdf, 0.5f * phi2);                  // Phi + x phi
+    }
+};
+
+struct GeluTanh {
+    template <bool Exact>
+    __device__ __forceinline__ static float fwd(float x)
+    {
+        float lo;
+        float w = tanh_arg<Exact>(x, &lo);
+        SigmoidParts p = sigmoid_parts(w);
+        float s = p.s;
+        if (Exact) s = fmaf(s * p.sm, lo, s);              // sigmoid(w + lo)
+        return x * s;
+    }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        float lo;
+        float w = tanh_arg<Exact>(x, &lo);
+        SigmoidParts p = sigmoid_parts(w);
+        float s = p.s;
+        if (Exact) s = fmaf(s * p.sm, lo, s);
+        // Beyond |x| = 1e4 either 1 - sigmoid(w) or sigmoid(w) is exactly 0, so
+        // clamping x inside the bracket leaves act' unchanged and keeps it finite.
+        float xc = fminf(fmaxf(x, -1.0e4f), 1.0e4f);
+        float dw = fmaf(3.0f * kC3Hi, xc * xc, kC1Hi);      // w'(x) = C1 + 3 C3 x^2
+        *act = x * s;
+        // d/dx [x sigmoid(w)] = sigmoid(w) (1 + x (1 - sigmoid(w)) w')
+        *dact = s * fmaf(xc * p.sm, dw, 1.0f);
+    }
+};
+
+struct Relu {
+    template <bool Exact>
+    __device__ __forceinline__ static float fwd(float x)
+    {
+        return x > 0.0f ? x : (x != x ? x : 0.0f);          // NaN propagates
+    }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        *act = x > 0.0f ? x : (x != x ? x : 0.0f);
+        *dact = x > 0.0f ? 1.0f : (x != x ? x : 0.0f);      // 0 at x == 0
+    }
+};
+
+}  // namespace glu

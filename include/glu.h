@@ -1,0 +1,194 @@
+/*
+ * glu.h - C ABI of the fused gated-activation library (GB300, sm_103a).
+ *
+ * The library computes the activation step of a gated MLP,
+ *
+ *     y = act(a) * b                                   (forward)
+ *     da = dc * act'(a) * b,   db = dc * act(a)        (backward)
+ *
+ * element by element, where a is the gate projection's output, b the up
+ * projection's output and dc the gradient arriving at y.  Sources:
+ *   - "Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel": Purpose (y = silu(a)*b
+ *     between the gate/up and down projections; GeGLU and ReGLU on the same
+ *     skeleton), Required reasoning process steps 1-9 (fp32 activation, cast at
+ *     the store, the GeGLU erf form, the [gate | up] layout, the backward),
+ *     Common failure modes (the tanh form of GELU, in-place over b, strides
+ *     from tensor metadata).
+ *   - "Kernel Profile: SwiGLU (Tier 1 - Element-wise)": Backward Pass
+ *     (gradient formulas, sigmoid recomputed from a) and Key Patterns (in-place
+ *     backward into a and b, no intermediate allocations).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers into memory the caller owns.  The
+ *     library allocates nothing, keeps no pointer after the call returns, and
+ *     is asynchronous: work is enqueued on `stream` (NULL = the legacy default
+ *     stream) and the call returns before it runs.
+ *   - Matrices are row-major with a contiguous last dimension: element (r, c)
+ *     of operand X is at X + r * X_stride + c.  Strides are in ELEMENTS of
+ *     `dtype`, not bytes, and are ignored when n_rows == 1.
+ *   - Every operand has the same dtype; outputs have the input dtype.  The
+ *     activation runs in fp32 and the result is rounded to nearest-even once,
+ *     at the store.  No flush-to-zero.
+ *   - An output may be exactly the same matrix as an input (same pointer, same
+ *     stride): each element's inputs are read before its outputs are written,
+ *     and no two threads touch the same element.  Any other overlap between an
+ *     output and an input, or any overlap between two outputs, is rejected
+ *     with GLU_ERR_ALIAS.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     negative return means nothing was enqueued.  n_rows == 0 or n_cols == 0
+ *     returns GLU_OK without launching (pointers may then be NULL).
+ *   - Pointers and strides that are 32- or 16-byte aligned use 256- or 128-bit
+ *     memory accesses; any other alignment is valid and uses element-wide
+ *     accesses.  Alignment is never an error.
+ *   - Non-finite inputs are outside the numerical contract; they do not fault.
+ */
+#ifndef GLU_H
+#define GLU_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GLU_VERSION 1
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *glu_stream_t;
+
+/* Activation applied to the gate operand a (never to b).
+ *   SILU       silu(x) = x * sigmoid(x)
+ *              ("Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel", step 5)
+ *   GELU_ERF   0.5 * x * (1 + erf(x / sqrt 2))                          (step 7)
+ *   GELU_TANH  0.5 * x * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))
+ *              (Common failure modes, "GELU variant mismatch")
+ *   RELU       max(x, 0); its derivative is taken as 0 at x == 0 (Purpose). */
+typedef enum {
+    GLU_ACT_SILU = 0,
+    GLU_ACT_GELU_ERF = 1,
+    GLU_ACT_GELU_TANH = 2,
+    GLU_ACT_RELU = 3
+} glu_act_t;
+
+/* SPLIT:  a and b are separate n_rows x n_cols matrices.
+ * CONCAT: one matrix x of n_rows x (2*n_cols) holds [gate | up] per row:
+ *         a = x[:, :n_cols], b = x[:, n_cols:2*n_cols]
+ *         ("Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel", Inputs item 4 and
+ *         Required reasoning step 8; the gate half comes first). */
+typedef enum {
+    GLU_LAYOUT_SPLIT = 0,
+    GLU_LAYOUT_CONCAT = 1
+} glu_layout_t;
+
+typedef enum {
+    GLU_F32 = 0,
+    GLU_F16 = 1,
+    GLU_BF16 = 2
+} glu_dtype_t;
+
+typedef enum {
+    GLU_OK = 0,
+    GLU_ERR_NULL = -1,    /* a required pointer is NULL (with n_rows, n_cols > 0) */
+    GLU_ERR_SHAPE = -2,   /* negative size, or a size whose byte extent overflows */
+    GLU_ERR_STRIDE = -3,  /* a stride smaller than its row width, or negative */
+    GLU_ERR_ALIAS = -4,   /* outputs overlap inputs other than exactly, or each other */
+    GLU_ERR_ENUM = -5,    /* unknown act, layout or dtype */
+    GLU_ERR_CUDA = -6     /* the CUDA runtime refused the launch; see glu_last_cuda_error() */
+} glu_status_t;
+
+/*
+ * Forward: y[r, c] = round(act(a[r, c]) * b[r, c]) for r < n_rows, c < n_cols.
+ *
+ *   a, a_stride   SPLIT: gate matrix.  CONCAT: the x matrix (width 2*n_cols,
+ *                 a_stride >= 2*n_cols); the gate is its first half.
+ *   b, b_stride   SPLIT: up matrix (b_stride >= n_cols).  CONCAT: ignored
+ *                 (the up half is x + n_cols with x's stride); pass NULL, 0.
+ *   y, y_stride   output, n_rows x n_cols, y_stride >= n_cols.  In place over
+ *                 the up operand: y = b, y_stride = b_stride (SPLIT) or
+ *                 y = x + n_cols, y_stride = a_stride (CONCAT).
+ *   stream        CUDA stream the kernel is enqueued on.
+ * Returns GLU_OK or a negative glu_status_t.
+ */
+int glu_fwd(const void *a, int64_t a_stride,
+            const void *b, int64_t b_stride,
+            void *y, int64_t y_stride,
+            int64_t n_rows, int64_t n_cols,
+            glu_layout_t layout, glu_act_t act, glu_dtype_t dtype,
+            glu_stream_t stream);
+
+/*
+ * Backward ("Kernel Profile: SwiGLU", Backward Pass):
+ *   da[r, c] = round(dc[r, c] * act'(a[r, c]) * b[r, c])
+ *   db[r, c] = round(dc[r, c] * act(a[r, c]))
+ * act and act' are recomputed in fp32 from a; nothing is saved by the forward.
+ *
+ *   dc, dc_stride incoming gradient, n_rows x n_cols.
+ *   a, b          as in glu_fwd (CONCAT: a is x, b is ignored).
+ *   da, da_stride SPLIT: gradient of a.  CONCAT: the dx matrix (width
+ *                 2*n_cols, da_stride >= 2*n_cols); da fills its first half and
+ *                 db its second.  In place ("Key Patterns", in-place backward):
+ *                 da = a with da_stride = a_stride (CONCAT: dx = x).
+ *   db, db_stride SPLIT: gradient of b; in place: db = b, db_stride = b_stride.
+ *                 CONCAT: ignored (db is dx + n_cols); pass NULL, 0.
+ * Returns GLU_OK or a negative glu_status_t.
+ */
+int glu_bwd(const void *dc, int64_t dc_stride,
+            const void *a, int64_t a_stride,
+            const void *b, int64_t b_stride,
+            void *da, int64_t da_stride,
+            void *db, int64_t db_stride,
+            int64_t n_rows, int64_t n_cols,
+            glu_layout_t layout, glu_act_t act, glu_dtype_t dtype,
+            glu_stream_t stream);
+
+/* Static English text for a glu_status_t value; never NULL. */
+const char *glu_status_string(int status);
+
+/* Text of the CUDA error behind this thread's most recent GLU_ERR_CUDA, or ""
+ * if there was none.  Valid until the next call on the same thread. */
+const char *glu_last_cuda_error(void);
+
+/* GLU_VERSION of the loaded library. */
+int glu_version(void);
+
+/* What this thread's most recent successful glu_fwd / glu_bwd enqueued.
+ * `launched` is 0 when the call was a no-op (an empty matrix). */
+typedef struct {
+    int32_t launched;     /* 1 if a kernel was enqueued */
+    int32_t backward;     /* 0 = forward kernel, 1 = backward kernel */
+    int32_t vec_bytes;    /* bytes per operand per memory access: 32, 16 or the element size */
+    int32_t unroll;       /* accesses each thread keeps in flight per operand */
+    int32_t threads;      /* threads per block */
+    int32_t grid;         /* blocks launched */
+    int32_t flattened;    /* 1 if the rows were contiguous and walked as one row */
+    int32_t reserved;
+    int64_t vector_units; /* full-width accesses per operand */
+    int64_t tail_elems;   /* elements handled one at a time (row ends) */
+} glu_launch_info_t;
+
+/* Copies this thread's last launch description into *out.  GLU_ERR_NULL if out is NULL. */
+int glu_last_launch(glu_launch_info_t *out);
+
+/* Process-wide launch tuning (used by benchmarks and tuning sweeps; the
+ * defaults are what the library was tuned to).  A field left at 0 means
+ * "library default".  Not synchronised with concurrent glu_fwd/glu_bwd calls
+ * on other threads.
+ *   vec_bytes     upper bound on the access width: 32, 16, or the element size
+ *   unroll        1, 2 or 4 accesses in flight per operand per thread
+ *   ctas_per_sm   >0: persistent grid of that many blocks per SM;
+ *                 <0: one block per tile of work (no grid-stride reuse) */
+typedef struct {
+    int32_t vec_bytes;
+    int32_t unroll;
+    int32_t ctas_per_sm;
+    int32_t reserved;
+} glu_tuning_t;
+
+int glu_set_tuning(const glu_tuning_t *t);   /* GLU_ERR_ENUM for unsupported values */
+int glu_get_tuning(glu_tuning_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLU_H */

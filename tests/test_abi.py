@@ -1,0 +1,201 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/glu.h
+declares, and its host-side validation returns the documented status codes.
+
+No test here enqueues GPU work.  Fake device addresses are only ever passed to
+calls that must be rejected before any launch; the one test that lets a valid
+call reach the CUDA runtime is skipped whenever a GPU is present."""
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import glu_activation_mlps_gb300 as glu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "glu.h")
+
+OK, NULL, SHAPE, STRIDE, ALIAS, ENUM, CUDA = 0, -1, -2, -3, -4, -5, -6
+SPLIT, CONCAT = 0, 1
+SILU, RELU = 0, 3
+F32, F16, BF16 = 0, 1, 2
+BASE = 1 << 32          # fake, 4 KiB-aligned device addresses: never dereferenced
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    glu.build()
+    glu.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(glu_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert set(names) == set(glu.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", glu.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (glu_\w+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(glu.lib(), n)
+
+
+def test_version_matches_header():
+    v = int(re.search(r"#define GLU_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert glu.glu_version() == v
+
+
+def test_status_strings():
+    for s in (OK, NULL, SHAPE, STRIDE, ALIAS, ENUM, CUDA):
+        assert glu.glu_status_string(s) and glu.glu_status_string(s) != "unknown status"
+    assert glu.glu_status_string(12345) == "unknown status"
+
+
+def fwd(a=BASE, sa=64, b=BASE + (1 << 20), sb=64, y=BASE + (2 << 20), sy=64,
+        rows=4, cols=64, layout=SPLIT, act=SILU, dtype=BF16):
+    return glu.glu_fwd(a, sa, b, sb, y, sy, rows, cols, layout, act, dtype, None)
+
+
+def bwd(dc=BASE + (3 << 20), sdc=64, a=BASE, sa=64, b=BASE + (1 << 20), sb=64,
+        da=BASE + (4 << 20), sda=64, db=BASE + (5 << 20), sdb=64, rows=4, cols=64,
+        layout=SPLIT, act=SILU, dtype=BF16):
+    return glu.glu_bwd(dc, sdc, a, sa, b, sb, da, sda, db, sdb, rows, cols, layout, act, dtype, None)
+
+
+def test_bad_enums():
+    assert fwd(layout=2) == ENUM
+    assert fwd(act=4) == ENUM and fwd(act=-1) == ENUM
+    assert fwd(dtype=3) == ENUM
+    assert bwd(layout=7) == ENUM and bwd(act=9) == ENUM and bwd(dtype=-2) == ENUM
+
+
+def test_shapes():
+    assert fwd(rows=-1) == SHAPE and fwd(cols=-5) == SHAPE
+    assert bwd(rows=-1) == SHAPE
+    # byte extent overflow
+    assert fwd(rows=1 << 40, sa=1 << 30, sb=1 << 30, sy=1 << 30, cols=1 << 30) == SHAPE
+
+
+def test_empty_is_a_noop_even_with_null_pointers():
+    assert fwd(a=None, b=None, y=None, rows=0) == OK
+    assert fwd(a=None, b=None, y=None, cols=0) == OK
+    assert bwd(dc=None, a=None, b=None, da=None, db=None, rows=0) == OK
+    assert glu.glu_last_launch()["launched"] == 0
+
+
+def test_null_pointers():
+    assert fwd(a=None) == NULL and fwd(b=None) == NULL and fwd(y=None) == NULL
+    assert fwd(b=None, layout=CONCAT, sa=128) != NULL          # b is ignored for CONCAT
+    for k in ("dc", "a", "b", "da", "db"):
+        assert bwd(**{k: None}) == NULL, k
+
+
+def test_strides():
+    assert fwd(sa=63) == STRIDE and fwd(sb=10) == STRIDE and fwd(sy=0) == STRIDE
+    assert fwd(sa=-64) == STRIDE
+    assert fwd(layout=CONCAT, sa=127) == STRIDE                 # x holds 2 * n_cols per row
+    assert bwd(sdc=63) == STRIDE and bwd(sdb=1) == STRIDE
+    assert bwd(layout=CONCAT, sa=128, sda=127) == STRIDE
+
+
+def test_partial_aliasing_is_rejected():
+    # y shifted by one element against b
+    assert fwd(y=BASE + (1 << 20) + 2) == ALIAS
+    # y == b but with another stride
+    assert fwd(b=BASE + (1 << 20), sb=64, y=BASE + (1 << 20), sy=128) == ALIAS
+    # y overlapping a by one row
+    assert fwd(y=BASE + 64 * 2) == ALIAS
+    # two backward outputs overlapping
+    assert bwd(da=BASE + (4 << 20), db=BASE + (4 << 20) + 32) == ALIAS
+    assert bwd(da=BASE + (4 << 20), db=BASE + (4 << 20)) == ALIAS
+    # CONCAT: y over the gate half is a partial overlap of x's rows
+    assert fwd(layout=CONCAT, sa=128, y=BASE + 2, sy=128) == ALIAS
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake addresses")
+def test_valid_calls_reach_the_cuda_runtime_without_a_gpu():
+    """Exact aliasing and interleaved-but-disjoint rows pass validation; with no
+    GPU the launch then fails cleanly with GLU_ERR_CUDA and a message."""
+    cases = [
+        fwd(),                                                   # out of place
+        fwd(y=BASE + (1 << 20)),                                 # in place over b
+        fwd(y=BASE, sy=64),                                      # in place over a
+        fwd(layout=CONCAT, sa=128, b=None, sb=0, y=BASE + 128, sy=128),   # y = x[:, I:]
+        fwd(b=BASE + 128, sa=256, sb=256, y=BASE + 256, sy=256),         # rows interleave
+        bwd(da=BASE, db=BASE + (1 << 20)),                       # in place backward
+        bwd(layout=CONCAT, sa=128, b=None, sb=0, da=BASE, sda=128, db=None, sdb=0),
+    ]
+    assert cases == [CUDA] * len(cases)
+    assert glu.glu_last_cuda_error()
+
+
+def test_tuning_roundtrip_and_validation():
+    glu.glu_set_tuning(16, 4, 8)
+    assert glu.glu_get_tuning() == {"vec_bytes": 16, "unroll": 4, "ctas_per_sm": 8}
+    for bad in ((8, 0, 0), (0, 3, 0), (0, 0, 100)):
+        with pytest.raises(glu.GluError):
+            glu.glu_set_tuning(*bad)
+    glu.glu_set_tuning(0, 0, 0)
+    assert glu.glu_get_tuning() == {"vec_bytes": 0, "unroll": 0, "ctas_per_sm": 0}
+
+
+def test_last_launch_requires_pointer():
+    assert glu.lib().glu_last_launch(None) == NULL
+
+
+FASTDIV_DRIVER = r"""
+#include <cstdio>
+#include <cstdint>
+#include "glu_plan.h"
+int main() {
+    const uint32_t ds[] = {1u, 2u, 3u, 7u, 10u, 11u, 250u, 688u, 1376u, 1792u, 2368u, 4096u,
+                           65535u, 65536u, 1000003u, 2147483647u, 2147483648u, 2147483649u,
+                           4294967295u};
+    const uint32_t ns[] = {0u, 1u, 2u, 3u, 99u, 65535u, 65536u, 123456789u, 2147483647u,
+                           2147483648u, 3000000000u, 4294967294u, 4294967295u};
+    unsigned long long bad = 0, checked = 0;
+    for (uint32_t d : ds) {
+        uint32_t m, s;
+        glu::fastdiv_init(d, &m, &s);
+        for (uint32_t n : ns) { ++checked; if (glu::fastdiv(n, m, s) != n / d) ++bad; }
+        uint64_t x = 88172645463325252ull;
+        for (int i = 0; i < 200000; ++i) {
+            x ^= x << 13; x ^= x >> 7; x ^= x << 17;
+            uint32_t n = uint32_t(x);
+            ++checked; if (glu::fastdiv(n, m, s) != n / d) ++bad;
+            uint32_t k = uint32_t(x >> 32) % 4096u;       // exact multiples and neighbours
+            uint64_t mult = uint64_t(k) * d;
+            if (mult + 1 <= 0xFFFFFFFFull) {
+                uint32_t a = uint32_t(mult), b = uint32_t(mult + 1);
+                checked += 2;
+                if (glu::fastdiv(a, m, s) != a / d) ++bad;
+                if (glu::fastdiv(b, m, s) != b / d) ++bad;
+                if (a) { ++checked; if (glu::fastdiv(a - 1, m, s) != (a - 1) / d) ++bad; }
+            }
+        }
+    }
+    printf("%llu %llu\n", checked, bad);
+    return bad != 0;
+}
+"""
+
+
+def test_fastdiv_host_logic(tmp_path):
+    """The multiply-shift division the kernels use to map a unit index to its
+    row, checked against integer division on the host."""
+    src = tmp_path / "fd.cpp"
+    src.write_text(FASTDIV_DRIVER)
+    exe = tmp_path / "fd"
+    csrc = os.path.join(ROOT, "glu_activation_mlps_gb300", "csrc")
+    cuda_inc = "/usr/local/cuda/include"
+    subprocess.run(["g++", "-O2", "-std=c++17", f"-I{csrc}", f"-I{cuda_inc}", str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    checked, bad = map(int, out.stdout.split())
+    assert out.returncode == 0 and bad == 0 and checked > 1_000_000
