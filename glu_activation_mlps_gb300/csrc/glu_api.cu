@@ -18,14 +18,16 @@ using glu::Params;
 thread_local glu_launch_info_t t_last_launch{};
 thread_local char t_cuda_error[256] = "";
 
-// Process-wide tuning; 0 = library default.  Defaults: 32-byte accesses where
-// the operands allow it, two accesses per operand in flight per thread, and a
-// grid of one block per tile (no persistent reuse).
+// Process-wide tuning; 0 = library default.  Defaults, per direction, from a
+// sweep on GB300 (4096 x 14336 bf16): the forward reads 2 and writes 1 operand
+// and is fastest with one 32-byte access per operand per thread; the backward
+// reads 3 and writes 2 and is fastest with two 16-byte accesses.  Both use one
+// block per tile (no persistent reuse).
 std::atomic<int32_t> g_vec_bytes{0};
 std::atomic<int32_t> g_unroll{0};
 std::atomic<int32_t> g_ctas_per_sm{0};
-constexpr int32_t kDefaultVecBytes = 32;
-constexpr int32_t kDefaultUnroll = 2;
+constexpr int32_t kDefaultVecBytes[2] = {32, 16};   // [forward, backward]
+constexpr int32_t kDefaultUnroll[2] = {1, 2};
 constexpr int32_t kDefaultCtasPerSm = -1;
 
 constexpr int kMaxDevices = 64;
@@ -150,7 +152,7 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
 
     // Widest access every operand's rows are aligned to.
     int32_t cap = g_vec_bytes.load(std::memory_order_relaxed);
-    if (cap == 0) cap = kDefaultVecBytes;
+    if (cap == 0) cap = kDefaultVecBytes[c.dir];
     int vb = 0;
     for (int cand : {32, 16}) {
         if (cand > cap) continue;
@@ -162,7 +164,7 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
         if (ok) { vb = cand; break; }
     }
     int32_t unroll = g_unroll.load(std::memory_order_relaxed);
-    if (unroll == 0) unroll = kDefaultUnroll;
+    if (unroll == 0) unroll = kDefaultUnroll[c.dir];
     const int unroll_sel = unroll == 1 ? 0 : (unroll == 2 ? 1 : 2);
     const int vb_sel = vb == 32 ? 0 : (vb == 16 ? 1 : 2);
     if (vb == 0) unroll = 1;

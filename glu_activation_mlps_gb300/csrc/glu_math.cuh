@@ -18,12 +18,23 @@
 //   1 + erf(z)          = erfc(-z)              (no cancellation for z < 0)
 //   0.5 (1 + tanh(u))   = sigmoid(2u)           (no cancellation for u < 0)
 //
+// Near the root x* of act' (silu' at -1.2785, both GELU' near -0.752) the two
+// terms of act' cancel, and the absolute error of any fp32 evaluation of them
+// (~1e-8) becomes a large relative error of act' itself.  Within |x - x*| <
+// 2^-7 act' is therefore taken from its Taylor series about x*, evaluated in
+// u = x - x* (exact in fp32 there, by Sterbenz's lemma): the series has no
+// cancellation, and its truncation error at degree 4 is ~1e-10 relative.  The
+// coefficients are act^(k+1)(x*)/k!, from the closed forms above.
+//
 // `Exact` selects the variant used when the storage dtype is fp32: there the
 // rounding of the scaled arguments (x/sqrt2, the tanh polynomial, x^2) would be
 // amplified by up to 2z^2 in the tails, so those arguments are carried as
 // (hi, lo) float pairs and the first-order effect of `lo` is applied
 // analytically.  For fp16/bf16 outputs the plain fp32 forms are far below
-// half an output ulp and the corrections are skipped.
+// half an output ulp and the corrections are skipped; there exp(-t) is taken
+// as 2^(-t log2 e) with the hardware base-2 exponential (ex2.approx, relative
+// error ~2^-22, subnormal results kept) and 1/(1+e), whose argument lies in
+// [1, 2], with the hardware reciprocal (rcp.approx, ~1 ulp).
 #pragma once
 #include <cuda_runtime.h>
 #include <math.h>
@@ -37,11 +48,32 @@ struct SigmoidParts {
     float sm;     // 1 - sigmoid(x) = sigmoid(-x), formed without cancellation
 };
 
+// e^(-t) for t >= 0.
+template <bool Exact>
+__device__ __forceinline__ float exp_neg(float t)
+{
+    if (Exact) return expf(-t);
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(t * -1.44269504f));   // -t log2(e)
+    return y;
+}
+
+// 1/d for d in [1, 2] (never subnormal, so flush-to-zero cannot change it).
+template <bool Exact>
+__device__ __forceinline__ float recip_1_2(float d)
+{
+    if (Exact) return __frcp_rn(d);
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
+    return y;
+}
+
+template <bool Exact>
 __device__ __forceinline__ SigmoidParts sigmoid_parts(float x)
 {
     SigmoidParts p;
-    p.e = expf(-fabsf(x));
-    p.r = __frcp_rn(1.0f + p.e);
+    p.e = exp_neg<Exact>(fabsf(x));
+    p.r = recip_1_2<Exact>(1.0f + p.e);
     float er = __fmul_rn(p.e, p.r);
     p.s = x >= 0.0f ? p.r : er;
     p.sm = x >= 0.0f ? er : p.r;
@@ -59,6 +91,35 @@ constexpr float kC1Hi = 1.59576917f;
 constexpr float kC1Lo = -4.53406805e-08f;
 constexpr float kC3Hi = 0.0713548139f;
 constexpr float kC3Lo = 2.39883247e-09f;
+
+// act'(x) = u (c1 + u (c2 + u (c3 + u c4))), u = x - x*, for |u| < kRootRadius.
+// x* = hi + lo (hi the nearest float).
+constexpr float kRootRadius = 0.0078125f;   // 2^-7
+struct RootSeries {
+    float hi, lo, c1, c2, c3, c4;
+};
+__host__ __device__ constexpr RootSeries silu_root()
+{
+    return {-1.27846456f, 1.29792825e-08f, 2.17811706e-01f,
+            1.46648797e-01f, 1.88748142e-02f, -1.52226552e-02f};
+}
+__host__ __device__ constexpr RootSeries gelu_erf_root()
+{
+    return {-0.751791537f, 1.21144499e-08f, 4.31493992e-01f,
+            3.88284983e-01f, -1.81996764e-02f, -1.14008233e-01f};
+}
+__host__ __device__ constexpr RootSeries gelu_tanh_root()
+{
+    return {-0.752461433f, 1.13396279e-08f, 4.30400091e-01f,
+            3.87518446e-01f, -1.57828535e-02f, -1.13944483e-01f};
+}
+
+// Replaces *dact by the series when x is within kRootRadius of the root.
+__device__ __forceinline__ void root_series(float x, const RootSeries r, float *dact)
+{
+    const float u = __fsub_rn(__fsub_rn(x, r.hi), r.lo);
+    if (fabsf(u) < kRootRadius) *dact = u * fmaf(u, fmaf(u, fmaf(u, r.c4, r.c3), r.c2), r.c1);
+}
 
 // erfc(-x / sqrt 2), the 2 Phi(x) of the GeGLU erf form.
 template <bool Exact>
@@ -107,17 +168,18 @@ struct Silu {
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
-        SigmoidParts p = sigmoid_parts(x);
+        SigmoidParts p = sigmoid_parts<Exact>(x);
         return x * p.s;
     }
     template <bool Exact>
     __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
     {
-        SigmoidParts p = sigmoid_parts(x);
+        SigmoidParts p = sigmoid_parts<Exact>(x);
         *act = x * p.s;
         float num = x >= 0.0f ? fmaf(x, p.e, 1.0f + p.e)      // 1 + e + x e
                               : p.e * ((1.0f + x) + p.e);     // e (1 + x + e)
         *dact = num * (p.r * p.r);
+        root_series(x, silu_root(), dact);
     }
 };
 
@@ -133,11 +195,12 @@ struct GeluErf {
         float phi2 = two_phi<Exact>(x);                     // 2 Phi(x)
         float ax = fminf(fabsf(x), 40.0f);                  // phi(40) is 0 in fp32
         float p = __fmul_rn(ax, ax);
-        float g = expf(-0.5f * p);
+        float g = exp_neg<Exact>(0.5f * p);
         if (Exact) g = g * (1.0f - 0.5f * fmaf(ax, ax, -p));  // x^2 = p + pe
         float pdf = kInvSqrt2Pi * g;                        // phi(x)
         *act = 0.5f * x * phi2;
         *dact = fmaf(x, pdf, 0.5f * phi2);                  // Phi + x phi
+        root_series(x, gelu_erf_root(), dact);
     }
 };
 
@@ -147,7 +210,7 @@ struct GeluTanh {
     {
         float lo;
         float w = tanh_arg<Exact>(x, &lo);
-        SigmoidParts p = sigmoid_parts(w);
+        SigmoidParts p = sigmoid_parts<Exact>(w);
         float s = p.s;
         if (Exact) s = fmaf(s * p.sm, lo, s);              // sigmoid(w + lo)
         return x * s;
@@ -157,7 +220,7 @@ struct GeluTanh {
     {
         float lo;
         float w = tanh_arg<Exact>(x, &lo);
-        SigmoidParts p = sigmoid_parts(w);
+        SigmoidParts p = sigmoid_parts<Exact>(w);
         float s = p.s;
         if (Exact) s = fmaf(s * p.sm, lo, s);
         // Beyond |x| = 1e4 either 1 - sigmoid(w) or sigmoid(w) is exactly 0, so
@@ -167,6 +230,7 @@ struct GeluTanh {
         *act = x * s;
         // d/dx [x sigmoid(w)] = sigmoid(w) (1 + x (1 - sigmoid(w)) w')
         *dact = s * fmaf(xc * p.sm, dw, 1.0f);
+        root_series(x, gelu_tanh_root(), dact);
     }
 };
 

@@ -1,8 +1,8 @@
 """Brute force over the whole input domain of the activation: every finite
 bf16 and f16 value of a, with b and dc fixed to a few values, forward and
 backward, all activations, against the oracle under the 1-ulp bar.  For f32,
-a dense sweep of a over |a| <= 80 (where results are normal fp32 numbers),
-denser still around the derivative roots and in the tails, under 1e-6*M.
+a dense sweep of a over [-200, 80], denser still around the derivative roots
+and in the tails, under the fp32 bar.
 Non-finite and extreme inputs only have to run without faulting and keep
 their sign/NaN behaviour."""
 import numpy as np
@@ -54,38 +54,32 @@ def test_every_16bit_input(orc, act, dt):
     assert all(s["max_ulp"] <= 1 for s in worst.values())
 
 
-# Lower end of the f32 sweep per activation: below it the exact result, or the
-# fp32 intermediate it is formed from (exp(-|w|), erfc), is no longer a normal
-# fp32 number, and a relative bar on fp32 no longer has a meaning.  That range
-# is covered by the sign / magnitude check further down.
-F32_LOW = {"silu": -80.0, "relu": -80.0, "gelu_erf": -12.5, "gelu_tanh": -9.5}
-
-
-def f32_grid(lo):
+def f32_grid():
     rng = np.random.default_rng(77)
     parts = [
-        np.linspace(lo, 80, 400001),
+        np.linspace(-200, 80, 600001),
         rng.uniform(-8, 8, 400000),
-        -1.2784645427610738 + np.linspace(-1e-3, 1e-3, 20001),     # silu' root
-        -0.7517915246935645 + np.linspace(-1e-3, 1e-3, 20001),     # gelu-erf' root
-        -0.7524614220710163 + np.linspace(-1e-3, 1e-3, 20001),     # gelu-tanh' root
-        np.geomspace(1e-30, 80, 20000), -np.geomspace(1e-30, -lo, 20000),
+        rng.uniform(-16, -6, 200000),                               # GELU tails
+        -1.2784645427610738 + np.linspace(-1e-2, 1e-2, 20001),     # silu' root
+        -0.7517915246935645 + np.linspace(-1e-2, 1e-2, 20001),     # gelu-erf' root
+        -0.7524614220710163 + np.linspace(-1e-2, 1e-2, 20001),     # gelu-tanh' root
+        np.geomspace(1e-30, 80, 20000), -np.geomspace(1e-30, 200, 20000),
     ]
-    x = np.concatenate(parts)
-    x = x[x >= lo].astype(np.float32)
-    return x.view(np.uint32)
+    return np.concatenate(parts).astype(np.float32).view(np.uint32)
 
 
 @pytest.mark.parametrize("act", ACTS)
 def test_dense_f32_sweep(orc, act):
-    a = f32_grid(F32_LOW[act])
+    """f32 a over [-200, 80] (deep tails included: there the fp32 bar's
+    absolute floor applies), denser near the derivative roots."""
+    a = f32_grid()
     n = a.size
     A = to_dev(a, "f32")
     for bv in (1.0, -3.5):
         b = const_bits(orc, "f32", bv, n)
         B = to_dev(b, "f32")
         y = glu.fwd(A, B, act=act)
-        compare(to_bits(y, "f32"), orc.fwd(act, "f32", a, b), "f32", what=f"{act} f32 fwd b={bv}")
+        st = compare(to_bits(y, "f32"), orc.fwd(act, "f32", a, b), "f32", what=f"{act} f32 fwd b={bv}")
         for cv in (1.0, 0.75):
             dc = const_bits(orc, "f32", cv, n)
             da, db = glu.bwd(to_dev(dc, "f32"), A, B, act=act)
@@ -93,21 +87,8 @@ def test_dense_f32_sweep(orc, act):
             scale = orc.bwd_da_scale(act, "f32", dc, a, b)
             compare(to_bits(da, "f32"), da_o, "f32", scale=scale, what=f"{act} f32 da b={bv}")
             compare(to_bits(db, "f32"), db_o, "f32", what=f"{act} f32 db b={bv}")
-
-
-@pytest.mark.parametrize("act", ACTS)
-def test_f32_deep_negative_tail(orc, act):
-    """Below the sweep's lower end the results are fp32 subnormals or zero:
-    they must be finite, carry no wrong sign and stay below the normal range."""
-    a = np.linspace(-200.0, F32_LOW[act], 20001).astype(np.float32).view(np.uint32)
-    b = const_bits(orc, "f32", 1.0, a.size)
-    A, B = to_dev(a, "f32"), to_dev(b, "f32")
-    y = to_bits(glu.fwd(A, B, act=act), "f32").view(np.float32)
-    da, db = glu.bwd(B, A, B, act=act)
-    for v in (y, to_bits(da, "f32").view(np.float32), to_bits(db, "f32").view(np.float32)):
-        assert np.isfinite(v).all()
-        assert (np.abs(v) < 2.0 ** -120).all()
-    assert (y <= 0).all()
+            v = to_bits(da, "f32").view(np.float32)
+            assert np.isfinite(v).all()
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
