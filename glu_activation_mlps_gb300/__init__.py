@@ -51,7 +51,7 @@ class LaunchInfo(ctypes.Structure):
 
 class Tuning(ctypes.Structure):
     _fields_ = [("vec_bytes", ctypes.c_int32), ("unroll", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("dependent_launch", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -127,8 +127,9 @@ def glu_last_launch() -> dict:
     return {f: getattr(info, f) for f, _ in LaunchInfo._fields_ if f != "reserved"}
 
 
-def glu_set_tuning(vec_bytes: int = 0, unroll: int = 0, ctas_per_sm: int = 0) -> None:
-    t = Tuning(vec_bytes, unroll, ctas_per_sm, 0)
+def glu_set_tuning(vec_bytes: int = 0, unroll: int = 0, ctas_per_sm: int = 0,
+                   dependent_launch: int = 0) -> None:
+    t = Tuning(vec_bytes, unroll, ctas_per_sm, dependent_launch)
     st = lib().glu_set_tuning(ctypes.byref(t))
     if st:
         raise GluError(st, "glu_set_tuning")
@@ -139,7 +140,8 @@ def glu_get_tuning() -> dict:
     st = lib().glu_get_tuning(ctypes.byref(t))
     if st:
         raise GluError(st, "glu_get_tuning")
-    return {"vec_bytes": t.vec_bytes, "unroll": t.unroll, "ctas_per_sm": t.ctas_per_sm}
+    return {"vec_bytes": t.vec_bytes, "unroll": t.unroll, "ctas_per_sm": t.ctas_per_sm,
+            "dependent_launch": t.dependent_launch}
 
 
 # ---- torch tensor marshalling -------------------------------------------------

@@ -26,6 +26,7 @@ thread_local char t_cuda_error[256] = "";
 std::atomic<int32_t> g_vec_bytes{0};
 std::atomic<int32_t> g_unroll{0};
 std::atomic<int32_t> g_ctas_per_sm{0};
+std::atomic<int32_t> g_dependent_launch{0};
 constexpr int32_t kDefaultVecBytes[2] = {32, 16};   // [forward, backward]
 constexpr int32_t kDefaultUnroll[2] = {1, 2};
 constexpr int32_t kDefaultCtasPerSm = -1;
@@ -208,9 +209,30 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
     }
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
 
+    // Launch with a programmatic dependency on the previous kernel in the
+    // stream (unless switched off): the kernel waits for that grid itself, so
+    // ordering and visibility are unchanged, but its blocks can be scheduled
+    // during the previous grid's tail.  If the runtime refuses the attribute,
+    // fall back to an ordinary launch.
     void *args[] = {&p};
-    cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(blocks)),
-                                     dim3(glu::kThreads), args, 0, stream);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(glu::kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const bool dependent = g_dependent_launch.load(std::memory_order_relaxed) >= 0;
+    cfg.attrs = dependent ? attr : nullptr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+    if (e != cudaSuccess && dependent) {
+        (void)cudaGetLastError();
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+    }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return cuda_fail(e);
@@ -357,13 +379,15 @@ int glu_last_launch(glu_launch_info_t *out)
 int glu_set_tuning(const glu_tuning_t *t)
 {
     if (!t) return GLU_ERR_NULL;
-    const int32_t v = t->vec_bytes, u = t->unroll, c = t->ctas_per_sm;
+    const int32_t v = t->vec_bytes, u = t->unroll, c = t->ctas_per_sm, d = t->dependent_launch;
     if (!(v == 0 || v == 32 || v == 16 || v == 4 || v == 2)) return GLU_ERR_ENUM;
     if (!(u == 0 || u == 1 || u == 2 || u == 4)) return GLU_ERR_ENUM;
     if (c > 64) return GLU_ERR_ENUM;
+    if (d < -1 || d > 1) return GLU_ERR_ENUM;
     g_vec_bytes.store(v);
     g_unroll.store(u);
     g_ctas_per_sm.store(c);
+    g_dependent_launch.store(d);
     return GLU_OK;
 }
 
@@ -373,7 +397,7 @@ int glu_get_tuning(glu_tuning_t *out)
     out->vec_bytes = g_vec_bytes.load();
     out->unroll = g_unroll.load();
     out->ctas_per_sm = g_ctas_per_sm.load();
-    out->reserved = 0;
+    out->dependent_launch = g_dependent_launch.load();
     return GLU_OK;
 }
 

@@ -199,6 +199,13 @@ __global__ void __launch_bounds__(kThreads) glu_kernel(const Params p)
     constexpr bool kExact = std::is_same<T, float>::value;
     using C = Codec<T>;
 
+    // Programmatic dependent launch: let the next kernel in the stream be
+    // scheduled while this grid's last blocks run, and do not touch memory
+    // before the previous grid has completed and its writes are visible.
+    // Both are no-ops when the launch carries no programmatic dependency.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     if constexpr (VB > 0) {
         constexpr int W = Access<VB>::W;
         constexpr int PW = C::kPerWord;

@@ -121,6 +121,39 @@ __device__ __forceinline__ void root_series(float x, const RootSeries r, float *
     if (fabsf(u) < kRootRadius) *dact = u * fmaf(u, fmaf(u, fmaf(u, r.c4, r.c3), r.c2), r.c1);
 }
 
+// Lower tail of the standard normal for bf16/f16 storage:
+//     Phi(-x) = exp(-x^2/2) * t * P(t),  t = 1/(1 + 0.3 x),  x >= 0,
+// with P of degree 7 fitted to the exact ratio (Mills' ratio form; relative
+// error of P <= 2.7e-6 in float32).  The coefficients are produced by
+// gen_phi_tail.py next to this file.  The exponential is returned too: it is
+// also sqrt(2 pi) phi(x), the density the GeGLU-erf backward needs.
+constexpr float kPhiTailC = 0.3f;
+__host__ __device__ constexpr float phi_tail_coef(int i)
+{
+    constexpr float p[8] = {1.196823716e-01f, 1.197295263e-01f, 1.077751145e-01f,
+                            9.759789705e-02f, 1.416620519e-02f, 1.230392978e-01f,
+                            -1.036966890e-01f, 2.170499042e-02f};
+    return p[i];
+}
+
+struct PhiTail {
+    float q;   // Phi(-x)
+    float e;   // exp(-x^2 / 2)
+};
+
+__device__ __forceinline__ PhiTail phi_tail(float x)   // x = |a| >= 0
+{
+    PhiTail r;
+    r.e = exp_neg<false>(0.5f * x * x);
+    float t;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(kPhiTailC, x, 1.0f)));   // t in (0, 1]
+    float p = phi_tail_coef(7);
+#pragma unroll
+    for (int i = 6; i >= 0; --i) p = fmaf(p, t, phi_tail_coef(i));
+    r.q = r.e * (t * p);
+    return r;
+}
+
 // erfc(-x / sqrt 2), the 2 Phi(x) of the GeGLU erf form.
 template <bool Exact>
 __device__ __forceinline__ float two_phi(float x)
@@ -187,11 +220,23 @@ struct GeluErf {
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
+        if (!Exact) {
+            const float q = phi_tail(fabsf(x)).q;          // Phi(-|x|)
+            return x * (x <= 0.0f ? q : 1.0f - q);          // x Phi(x)
+        }
         return 0.5f * x * two_phi<Exact>(x);
     }
     template <bool Exact>
     __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
     {
+        if (!Exact) {
+            const PhiTail t = phi_tail(fabsf(x));
+            const float cdf = x <= 0.0f ? t.q : 1.0f - t.q;  // Phi(x)
+            *act = x * cdf;
+            *dact = fmaf(x, kInvSqrt2Pi * t.e, cdf);        // Phi + x phi
+            root_series(x, gelu_erf_root(), dact);
+            return;
+        }
         float phi2 = two_phi<Exact>(x);                     // 2 Phi(x)
         float ax = fminf(fabsf(x), 40.0f);                  // phi(40) is 0 in fp32
         float p = __fmul_rn(ax, ax);

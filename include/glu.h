@@ -176,12 +176,17 @@ int glu_last_launch(glu_launch_info_t *out);
  *   vec_bytes     upper bound on the access width: 32, 16, or the element size
  *   unroll        1, 2 or 4 accesses in flight per operand per thread
  *   ctas_per_sm   >0: persistent grid of that many blocks per SM;
- *                 <0: one block per tile of work (no grid-stride reuse) */
+ *                 <0: one block per tile of work (no grid-stride reuse)
+ *   dependent_launch
+ *                 0 or 1: launch with a programmatic dependency on the previous
+ *                 kernel in the stream (the kernel still waits for that grid to
+ *                 finish before touching memory, so results and ordering are
+ *                 unchanged; only scheduling overlaps); -1: ordinary launch */
 typedef struct {
     int32_t vec_bytes;
     int32_t unroll;
     int32_t ctas_per_sm;
-    int32_t reserved;
+    int32_t dependent_launch;
 } glu_tuning_t;
 
 int glu_set_tuning(const glu_tuning_t *t);   /* GLU_ERR_ENUM for unsupported values */

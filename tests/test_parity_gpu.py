@@ -261,3 +261,49 @@ def test_activation_sweep_full_size(orc, H, dt):
         da_o, db_o = orc.bwd(act, dt, dc_s, a_s, b_s)
         compare(to_bits(da.view(-1)[idx_t], dt), da_o, dt, scale=scale, what=f"{act} {dt} H={H} da")
         compare(to_bits(db.view(-1)[idx_t], dt), db_o, dt, what=f"{act} {dt} H={H} db")
+
+
+# ---------------------------------------------------------------- dependent launches
+
+@pytest.mark.parametrize("dependent", [0, -1])
+def test_back_to_back_dependent_kernels(orc, dependent):
+    """A chain of launches on one stream in which every launch reads what the
+    previous one wrote (forward output -> next forward's gate, backward inputs
+    from the chain).  Values are signed powers of two and the activation is
+    ReLU, so every product is exact: the GPU chain must equal the oracle's
+    chain bit for bit, and any launch that read its input before the previous
+    kernel finished writing it would show up as a mismatch.  Run with and
+    without programmatic dependent launch."""
+    glu.glu_set_tuning(0, 0, 0, dependent)
+    try:
+        rows, cols, dt = 2048, 4096, "bf16"
+        rng = np.random.default_rng(99)
+        pick = np.array([-2.0, -1.0, -0.5, 0.5, 1.0, 2.0])
+        a = orc.encode(dt, rng.choice(pick, (rows, cols)))
+        b = orc.encode(dt, rng.choice(pick, (rows, cols)))
+        x_gpu, B = to_dev(a, dt), to_dev(b, dt)
+        x_orc = a
+        n = 40
+        # every output buffer starts as NaN and is allocated before the chain,
+        # so that only the library's kernels run back to back on the stream
+        bufs = [torch.full_like(x_gpu, float("nan")) for _ in range(n + n // 4)]
+        torch.cuda.synchronize()
+        outs = []
+        for k in range(n):
+            if k % 4 == 3:      # backward: dc = x, a = x  ->  da, db feed the chain
+                da, db = bufs.pop(), bufs.pop()
+                glu.bwd(x_gpu, x_gpu, B, da=da, db=db, act="relu")
+                da_o, db_o = orc.bwd("relu", dt, x_orc, x_orc, b)
+                x_gpu, x_orc = db, db_o
+                outs.append((da, da_o))
+            else:
+                y = bufs.pop()
+                glu.fwd(x_gpu, B, y=y, act="relu")
+                x_orc = orc.fwd("relu", dt, x_orc, b)
+                x_gpu = y
+        torch.cuda.synchronize()
+        assert np.array_equal(to_bits(x_gpu, dt), x_orc)
+        for g, o in outs:
+            assert np.array_equal(to_bits(g, dt), o)
+    finally:
+        glu.glu_set_tuning(0, 0, 0, 0)
