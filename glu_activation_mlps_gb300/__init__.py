@@ -25,11 +25,12 @@ ACT = {"silu": 0, "gelu_erf": 1, "gelu_tanh": 2, "relu": 3}
 LAYOUT = {"split": 0, "concat": 1}
 DTYPE = {"f32": 0, "f16": 1, "bf16": 2}
 STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STRIDE",
-          -4: "GLU_ERR_ALIAS", -5: "GLU_ERR_ENUM", -6: "GLU_ERR_CUDA"}
+          -4: "GLU_ERR_ALIAS", -5: "GLU_ERR_ENUM", -6: "GLU_ERR_CUDA", -7: "GLU_ERR_WORKSPACE"}
 
 # Every symbol include/glu.h declares.
-EXPORTS = ("glu_fwd", "glu_bwd", "glu_status_string", "glu_last_cuda_error", "glu_version",
-           "glu_last_launch", "glu_set_tuning", "glu_get_tuning")
+EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_host_workspace_bytes",
+           "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
+           "glu_set_tuning", "glu_get_tuning")
 
 
 class GluError(RuntimeError):
@@ -78,6 +79,14 @@ def lib() -> ctypes.CDLL:
             L.glu_fwd.restype = ci
             L.glu_bwd.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci, vp]
             L.glu_bwd.restype = ci
+            sz = ctypes.c_size_t
+            L.glu_fwd_host.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci, vp, sz, vp, vp, vp]
+            L.glu_fwd_host.restype = ci
+            L.glu_bwd_host.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci,
+                                       vp, sz, vp, vp, vp]
+            L.glu_bwd_host.restype = ci
+            L.glu_host_workspace_bytes.argtypes = [i64, i64, ci, ci, ci]
+            L.glu_host_workspace_bytes.restype = sz
             L.glu_status_string.argtypes = [ci]
             L.glu_status_string.restype = ctypes.c_char_p
             L.glu_last_cuda_error.argtypes = []
@@ -105,6 +114,23 @@ def glu_bwd(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_strid
             n_rows, n_cols, layout, act, dtype, stream) -> int:
     return lib().glu_bwd(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_stride,
                          n_rows, n_cols, layout, act, dtype, stream)
+
+
+def glu_fwd_host(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols, layout, act, dtype,
+                 workspace, workspace_bytes, copy_in, compute, copy_out) -> int:
+    return lib().glu_fwd_host(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols, layout, act, dtype,
+                              workspace, workspace_bytes, copy_in, compute, copy_out)
+
+
+def glu_bwd_host(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_stride, n_rows, n_cols,
+                 layout, act, dtype, workspace, workspace_bytes, copy_in, compute, copy_out) -> int:
+    return lib().glu_bwd_host(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_stride,
+                              n_rows, n_cols, layout, act, dtype, workspace, workspace_bytes,
+                              copy_in, compute, copy_out)
+
+
+def glu_host_workspace_bytes(rows_per_block, n_cols, layout, dtype, backward) -> int:
+    return lib().glu_host_workspace_bytes(rows_per_block, n_cols, layout, dtype, backward)
 
 
 def glu_status_string(status: int) -> str:
@@ -254,4 +280,87 @@ def bwd(dc, a, b=None, *, da=None, db=None, act: str = "silu", layout: str = "sp
                  LAYOUT[layout], ACT[act], code, _stream(stream))
     if st:
         raise GluError(st, "glu_bwd")
+    return da, db
+
+
+# ---- host tensors ---------------------------------------------------------------
+
+def _host_rows(t, name):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dim() == 1:
+        return 1, t.shape[0]
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    n = 1
+    for s_ in t.shape[:-1]:
+        n *= s_
+    return n, t.stride(-2)
+
+
+class HostPipeline:
+    """Device workspace and the three streams the host-memory entry points
+    use.  Allocation is torch's (plumbing); the copies and kernels are the
+    library's."""
+
+    def __init__(self, workspace_bytes: int = 256 << 20, device=None):
+        import torch
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        self.workspace = torch.empty(workspace_bytes, dtype=torch.uint8, device=dev)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+
+    def args(self, compute=None):
+        import torch
+        compute = torch.cuda.current_stream() if compute is None else compute
+        return (self.workspace.data_ptr(), self.workspace.numel(), self.copy_in.cuda_stream,
+                compute.cuda_stream, self.copy_out.cuda_stream)
+
+
+def fwd_host(pipe: HostPipeline, a, b=None, *, y=None, act="silu", layout="split", compute=None):
+    """glu_fwd_host on CPU tensors (page-locked for overlap).  Returns y (a CPU
+    tensor); synchronise the compute stream before reading it."""
+    import torch
+    concat = layout == "concat"
+    n_rows, a_stride = _host_rows(a, "a")
+    n_cols = a.shape[-1] // 2 if concat else a.shape[-1]
+    if y is None:
+        shape = (*a.shape[:-1], n_cols)
+        y = torch.empty(shape, dtype=a.dtype, pin_memory=a.is_pinned())
+    _, y_stride = _host_rows(y, "y")
+    b_ptr, b_stride = (None, 0) if concat else (b.data_ptr(), _host_rows(b, "b")[1])
+    st = glu_fwd_host(a.data_ptr(), a_stride, b_ptr, b_stride, y.data_ptr(), y_stride, n_rows, n_cols,
+                      LAYOUT[layout], ACT[act], _dtype_code(a), *pipe.args(compute))
+    if st:
+        raise GluError(st, "glu_fwd_host")
+    return y
+
+
+def bwd_host(pipe: HostPipeline, dc, a, b=None, *, da=None, db=None, act="silu", layout="split",
+             compute=None):
+    """glu_bwd_host on CPU tensors.  SPLIT returns (da, db); CONCAT returns dx."""
+    import torch
+    concat = layout == "concat"
+    n_rows, a_stride = _host_rows(a, "a")
+    _, dc_stride = _host_rows(dc, "dc")
+    n_cols = dc.shape[-1]
+    pin = a.is_pinned()
+    if da is None:
+        da = torch.empty(a.shape, dtype=a.dtype, pin_memory=pin)
+    _, da_stride = _host_rows(da, "da")
+    if concat:
+        st = glu_bwd_host(dc.data_ptr(), dc_stride, a.data_ptr(), a_stride, None, 0, da.data_ptr(), da_stride,
+                          None, 0, n_rows, n_cols, LAYOUT[layout], ACT[act], _dtype_code(a), *pipe.args(compute))
+        if st:
+            raise GluError(st, "glu_bwd_host")
+        return da
+    if db is None:
+        db = torch.empty(b.shape, dtype=b.dtype, pin_memory=pin)
+    _, b_stride = _host_rows(b, "b")
+    _, db_stride = _host_rows(db, "db")
+    st = glu_bwd_host(dc.data_ptr(), dc_stride, a.data_ptr(), a_stride, b.data_ptr(), b_stride, da.data_ptr(),
+                      da_stride, db.data_ptr(), db_stride, n_rows, n_cols, LAYOUT[layout], ACT[act],
+                      _dtype_code(a), *pipe.args(compute))
+    if st:
+        raise GluError(st, "glu_bwd_host")
     return da, db

@@ -13,23 +13,36 @@
 
 namespace {
 
+using glu::kBwd;
+using glu::kFwd;
 using glu::Params;
 
 thread_local glu_launch_info_t t_last_launch{};
 thread_local char t_cuda_error[256] = "";
 
-// Process-wide tuning; 0 = library default.  Defaults, per direction, from a
-// sweep on GB300 (4096 x 14336 bf16): the forward reads 2 and writes 1 operand
-// and is fastest with one 32-byte access per operand per thread; the backward
-// reads 3 and writes 2 and is fastest with two 16-byte accesses.  Both use one
-// block per tile (no persistent reuse).
+// Process-wide tuning; 0 = library default.
 std::atomic<int32_t> g_vec_bytes{0};
 std::atomic<int32_t> g_unroll{0};
 std::atomic<int32_t> g_ctas_per_sm{0};
 std::atomic<int32_t> g_dependent_launch{0};
-constexpr int32_t kDefaultVecBytes[2] = {32, 16};   // [forward, backward]
-constexpr int32_t kDefaultUnroll[2] = {1, 2};
-constexpr int32_t kDefaultCtasPerSm = -1;
+constexpr int32_t kDefaultCtasPerSm = -1;     // one block per tile
+
+// Default access width (bytes) and accesses in flight per operand per thread,
+// by [dtype][activation][direction], from a sweep on GB300 of 4096 x {4096,
+// 16384} matrices launched back to back: the forward of the heavier GELUs wants
+// two 32-byte accesses in flight (more arithmetic to hide), the SiLU and
+// GeGLU-tanh backward two 16-byte ones, ReGLU one 16-byte access.
+struct LaunchDefault {
+    int8_t vec_bytes, unroll;
+};
+constexpr LaunchDefault kDefaults[3][4][2] = {
+    // f32:  silu            gelu_erf         gelu_tanh        relu
+    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {32, 1}}, {{16, 1}, {16, 1}}},
+    // f16
+    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{16, 2}, {16, 1}}},
+    // bf16
+    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{16, 1}, {16, 1}}},
+};
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -118,21 +131,9 @@ int sm_count()
     return c;
 }
 
-int cuda_fail(cudaError_t e)
-{
-    snprintf(t_cuda_error, sizeof(t_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
-    return GLU_ERR_CUDA;
-}
+using glu::cuda_fail;
 
-// Everything the planner needs about one call after validation.  Strides are
-// in elements; ptrs/strides list every operand (inputs then outputs).
-struct Call {
-    int dir, act, dtype, E;
-    int64_t rows, cols;
-    const char *a, *b, *dc;
-    char *y0, *y1;
-    int64_t sa, sb, sdc, sy0, sy1;
-};
+using glu::Call;
 
 int plan_and_launch(const Call &c, cudaStream_t stream)
 {
@@ -153,7 +154,8 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
 
     // Widest access every operand's rows are aligned to.
     int32_t cap = g_vec_bytes.load(std::memory_order_relaxed);
-    if (cap == 0) cap = kDefaultVecBytes[c.dir];
+    const LaunchDefault dflt = kDefaults[c.dtype][c.act][c.dir];
+    if (cap == 0) cap = dflt.vec_bytes;
     int vb = 0;
     for (int cand : {32, 16}) {
         if (cand > cap) continue;
@@ -165,7 +167,7 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
         if (ok) { vb = cand; break; }
     }
     int32_t unroll = g_unroll.load(std::memory_order_relaxed);
-    if (unroll == 0) unroll = kDefaultUnroll[c.dir];
+    if (unroll == 0) unroll = dflt.unroll;
     const int unroll_sel = unroll == 1 ? 0 : (unroll == 2 ? 1 : 2);
     const int vb_sel = vb == 32 ? 0 : (vb == 16 ? 1 : 2);
     if (vb == 0) unroll = 1;
@@ -259,15 +261,22 @@ void mark_noop()
 
 }  // namespace
 
-extern "C" {
+namespace glu {
 
-int glu_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, void *y,
-            int64_t y_stride, int64_t n_rows, int64_t n_cols, glu_layout_t layout,
-            glu_act_t act, glu_dtype_t dtype, glu_stream_t stream)
+int cuda_fail(cudaError_t e)
 {
+    snprintf(t_cuda_error, sizeof(t_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return GLU_ERR_CUDA;
+}
+
+int validate_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, const void *y,
+                 int64_t y_stride, int64_t n_rows, int64_t n_cols, int layout, int act, int dtype,
+                 Call *c)
+{
+    *c = Call{};
     if (!valid_enums(layout, act, dtype)) return GLU_ERR_ENUM;
     if (n_rows < 0 || n_cols < 0) return GLU_ERR_SHAPE;
-    if (n_rows == 0 || n_cols == 0) { mark_noop(); return GLU_OK; }
+    if (n_rows == 0 || n_cols == 0) { c->empty = true; return GLU_OK; }
     const bool concat = layout == GLU_LAYOUT_CONCAT;
     if (!a || !y || (!concat && !b)) return GLU_ERR_NULL;
     const int E = elem_size(dtype);
@@ -275,6 +284,7 @@ int glu_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, vo
     if (concat) {
         if (n_cols > INT64_MAX / 2) return GLU_ERR_SHAPE;
         if (a_stride < 2 * n_cols) return GLU_ERR_STRIDE;
+        if (uintptr_t(a) > UINTPTR_MAX - uintptr_t(n_cols) * E) return GLU_ERR_SHAPE;
         b = static_cast<const char *>(a) + n_cols * E;
         b_stride = a_stride;
     } else if (a_stride < n_cols || b_stride < n_cols) {
@@ -289,25 +299,25 @@ int glu_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, vo
         extent_bytes(my, n_rows, E) < 0)
         return GLU_ERR_SHAPE;
     const Mat ins[2] = {ma, mb};
-    if (int s = check_aliasing(ins, 2, &my, 1, n_rows, E)) return s;
+    if (int st = check_aliasing(ins, 2, &my, 1, n_rows, E)) return st;
 
-    Call c{};
-    c.dir = glu::kFwd; c.act = act; c.dtype = dtype; c.E = E;
-    c.rows = n_rows; c.cols = n_cols;
-    c.a = static_cast<const char *>(a); c.b = static_cast<const char *>(b);
-    c.y0 = static_cast<char *>(y);
-    c.sa = a_stride; c.sb = b_stride; c.sy0 = y_stride;
-    return plan_and_launch(c, reinterpret_cast<cudaStream_t>(stream));
+    c->dir = kFwd; c->act = act; c->dtype = dtype; c->E = E;
+    c->rows = n_rows; c->cols = n_cols;
+    c->a = static_cast<const char *>(a); c->b = static_cast<const char *>(b);
+    c->y0 = static_cast<char *>(const_cast<void *>(y));
+    c->sa = a_stride; c->sb = b_stride; c->sy0 = y_stride;
+    return GLU_OK;
 }
 
-int glu_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
-            int64_t b_stride, void *da, int64_t da_stride, void *db, int64_t db_stride,
-            int64_t n_rows, int64_t n_cols, glu_layout_t layout, glu_act_t act,
-            glu_dtype_t dtype, glu_stream_t stream)
+int validate_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
+                 int64_t b_stride, const void *da, int64_t da_stride, const void *db,
+                 int64_t db_stride, int64_t n_rows, int64_t n_cols, int layout, int act, int dtype,
+                 Call *c)
 {
+    *c = Call{};
     if (!valid_enums(layout, act, dtype)) return GLU_ERR_ENUM;
     if (n_rows < 0 || n_cols < 0) return GLU_ERR_SHAPE;
-    if (n_rows == 0 || n_cols == 0) { mark_noop(); return GLU_OK; }
+    if (n_rows == 0 || n_cols == 0) { c->empty = true; return GLU_OK; }
     const bool concat = layout == GLU_LAYOUT_CONCAT;
     if (!dc || !a || !da || (!concat && (!b || !db))) return GLU_ERR_NULL;
     const int E = elem_size(dtype);
@@ -319,9 +329,12 @@ int glu_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, 
     if (concat) {
         if (n_cols > INT64_MAX / 2) return GLU_ERR_SHAPE;
         if (a_stride < 2 * n_cols || da_stride < 2 * n_cols) return GLU_ERR_STRIDE;
+        if (uintptr_t(a) > UINTPTR_MAX - uintptr_t(n_cols) * E ||
+            uintptr_t(da) > UINTPTR_MAX - uintptr_t(n_cols) * E)
+            return GLU_ERR_SHAPE;
         b = static_cast<const char *>(a) + n_cols * E;
         b_stride = a_stride;
-        db = static_cast<char *>(da) + n_cols * E;
+        db = static_cast<const char *>(da) + n_cols * E;
         db_stride = da_stride;
     } else if (a_stride < n_cols || b_stride < n_cols || da_stride < n_cols || db_stride < n_cols) {
         return GLU_ERR_STRIDE;
@@ -339,15 +352,44 @@ int glu_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, 
         return GLU_ERR_SHAPE;
     const Mat ins[3] = {mc, ma, mb};
     const Mat outs[2] = {mda, mdb};
-    if (int s = check_aliasing(ins, 3, outs, 2, n_rows, E)) return s;
+    if (int st = check_aliasing(ins, 3, outs, 2, n_rows, E)) return st;
 
-    Call c{};
-    c.dir = glu::kBwd; c.act = act; c.dtype = dtype; c.E = E;
-    c.rows = n_rows; c.cols = n_cols;
-    c.a = static_cast<const char *>(a); c.b = static_cast<const char *>(b);
-    c.dc = static_cast<const char *>(dc);
-    c.y0 = static_cast<char *>(da); c.y1 = static_cast<char *>(db);
-    c.sa = a_stride; c.sb = b_stride; c.sdc = dc_stride; c.sy0 = da_stride; c.sy1 = db_stride;
+    c->dir = kBwd; c->act = act; c->dtype = dtype; c->E = E;
+    c->rows = n_rows; c->cols = n_cols;
+    c->a = static_cast<const char *>(a); c->b = static_cast<const char *>(b);
+    c->dc = static_cast<const char *>(dc);
+    c->y0 = static_cast<char *>(const_cast<void *>(da));
+    c->y1 = static_cast<char *>(const_cast<void *>(db));
+    c->sa = a_stride; c->sb = b_stride; c->sdc = dc_stride; c->sy0 = da_stride; c->sy1 = db_stride;
+    return GLU_OK;
+}
+
+}  // namespace glu
+
+extern "C" {
+
+int glu_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, void *y,
+            int64_t y_stride, int64_t n_rows, int64_t n_cols, glu_layout_t layout,
+            glu_act_t act, glu_dtype_t dtype, glu_stream_t stream)
+{
+    Call c;
+    const int st = glu::validate_fwd(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols, layout,
+                                     act, dtype, &c);
+    if (st != GLU_OK) return st;
+    if (c.empty) { mark_noop(); return GLU_OK; }
+    return plan_and_launch(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int glu_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
+            int64_t b_stride, void *da, int64_t da_stride, void *db, int64_t db_stride,
+            int64_t n_rows, int64_t n_cols, glu_layout_t layout, glu_act_t act,
+            glu_dtype_t dtype, glu_stream_t stream)
+{
+    Call c;
+    const int st = glu::validate_bwd(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db,
+                                     db_stride, n_rows, n_cols, layout, act, dtype, &c);
+    if (st != GLU_OK) return st;
+    if (c.empty) { mark_noop(); return GLU_OK; }
     return plan_and_launch(c, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -360,7 +402,8 @@ const char *glu_status_string(int status)
     case GLU_ERR_STRIDE: return "a row stride is smaller than its row width";
     case GLU_ERR_ALIAS: return "an output overlaps an input other than exactly, or another output";
     case GLU_ERR_ENUM: return "unknown activation, layout, dtype or tuning value";
-    case GLU_ERR_CUDA: return "the CUDA runtime refused the launch";
+    case GLU_ERR_CUDA: return "the CUDA runtime refused a launch or copy";
+    case GLU_ERR_WORKSPACE: return "the workspace is NULL or too small for one row";
     default: return "unknown status";
     }
 }

@@ -68,4 +68,29 @@ KernelFn kernel_bf16(int act, int dir, int vb_sel, int unroll_sel);
 
 constexpr int kThreads = 256;
 
+// One validated call: what the planner needs.  Strides are in elements.
+struct Call {
+    int dir, act, dtype, E;
+    int64_t rows, cols;
+    const char *a, *b, *dc;
+    char *y0, *y1;
+    int64_t sa, sb, sdc, sy0, sy1;
+    bool empty;   // n_rows == 0 or n_cols == 0: nothing to do
+};
+
+// Argument rules of glu_fwd / glu_bwd (include/glu.h), shared by the device
+// and the host-memory entry points.  Pure host logic: no CUDA call.  On
+// GLU_OK, *c describes the call with the [gate | up] layout resolved into
+// separate operands.
+int validate_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_stride, const void *y,
+                 int64_t y_stride, int64_t n_rows, int64_t n_cols, int layout, int act, int dtype,
+                 Call *c);
+int validate_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
+                 int64_t b_stride, const void *da, int64_t da_stride, const void *db,
+                 int64_t db_stride, int64_t n_rows, int64_t n_cols, int layout, int act, int dtype,
+                 Call *c);
+
+// Records the text of a CUDA error for glu_last_cuda_error() and returns GLU_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+
 }  // namespace glu

@@ -45,6 +45,7 @@
 #ifndef GLU_H
 #define GLU_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -93,7 +94,8 @@ typedef enum {
     GLU_ERR_STRIDE = -3,  /* a stride smaller than its row width, or negative */
     GLU_ERR_ALIAS = -4,   /* outputs overlap inputs other than exactly, or each other */
     GLU_ERR_ENUM = -5,    /* unknown act, layout or dtype */
-    GLU_ERR_CUDA = -6     /* the CUDA runtime refused the launch; see glu_last_cuda_error() */
+    GLU_ERR_CUDA = -6,    /* the CUDA runtime refused a launch or copy; see glu_last_cuda_error() */
+    GLU_ERR_WORKSPACE = -7  /* host-memory entry points: workspace NULL or too small for one row */
 } glu_status_t;
 
 /*
@@ -140,6 +142,55 @@ int glu_bwd(const void *dc, int64_t dc_stride,
             int64_t n_rows, int64_t n_cols,
             glu_layout_t layout, glu_act_t act, glu_dtype_t dtype,
             glu_stream_t stream);
+
+/*
+ * Host-memory variants.  Same computation, arguments and rules as glu_fwd /
+ * glu_bwd (layouts, strides in elements, exact in-place aliasing, status
+ * codes), except that every matrix argument is a HOST pointer.  Blocks of
+ * rows are copied into `workspace`, processed by the same kernels, and copied
+ * back; two workspace slots alternate so that the copy in of one block, the
+ * kernel of the previous one and the copy out of the one before overlap.
+ *
+ *   workspace, workspace_bytes
+ *                 DEVICE memory owned by the caller, at least
+ *                 glu_host_workspace_bytes(1, ...) bytes (256-byte aligned is
+ *                 best).  More workspace means larger blocks and fewer copies;
+ *                 the library allocates nothing.  It must not be used by other
+ *                 work until the call's work has completed.
+ *   copy_in, compute, copy_out
+ *                 streams for the host-to-device copies, the kernels and the
+ *                 device-to-host copies.  They may be the same stream (no
+ *                 overlap).  Work already enqueued on `compute` is finished
+ *                 before the first copy; work enqueued on `compute` after the
+ *                 call runs after the last copy out, so synchronising `compute`
+ *                 is enough to see the outputs.
+ * Host memory that is not page-locked is valid but its copies do not overlap.
+ * On GLU_ERR_CUDA part of the work may have been enqueued and the outputs are
+ * unspecified.
+ */
+int glu_fwd_host(const void *a, int64_t a_stride,
+                 const void *b, int64_t b_stride,
+                 void *y, int64_t y_stride,
+                 int64_t n_rows, int64_t n_cols,
+                 glu_layout_t layout, glu_act_t act, glu_dtype_t dtype,
+                 void *workspace, size_t workspace_bytes,
+                 glu_stream_t copy_in, glu_stream_t compute, glu_stream_t copy_out);
+
+int glu_bwd_host(const void *dc, int64_t dc_stride,
+                 const void *a, int64_t a_stride,
+                 const void *b, int64_t b_stride,
+                 void *da, int64_t da_stride,
+                 void *db, int64_t db_stride,
+                 int64_t n_rows, int64_t n_cols,
+                 glu_layout_t layout, glu_act_t act, glu_dtype_t dtype,
+                 void *workspace, size_t workspace_bytes,
+                 glu_stream_t copy_in, glu_stream_t compute, glu_stream_t copy_out);
+
+/* Workspace bytes glu_fwd_host (backward == 0) or glu_bwd_host (backward != 0)
+ * needs for blocks of `rows_per_block` rows of `n_cols` columns; 0 for invalid
+ * arguments. */
+size_t glu_host_workspace_bytes(int64_t rows_per_block, int64_t n_cols, glu_layout_t layout,
+                                glu_dtype_t dtype, int backward);
 
 /* Static English text for a glu_status_t value; never NULL. */
 const char *glu_status_string(int status);

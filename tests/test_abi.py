@@ -199,3 +199,31 @@ def test_fastdiv_host_logic(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     checked, bad = map(int, out.stdout.split())
     assert out.returncode == 0 and bad == 0 and checked > 1_000_000
+
+
+def test_host_entry_points_validate_before_any_cuda_call():
+    WS = BASE + (8 << 20)
+    fh = lambda **k: glu.glu_fwd_host(*[k.get(n, d) for n, d in (
+        ("a", BASE), ("sa", 64), ("b", BASE + (1 << 20)), ("sb", 64), ("y", BASE + (2 << 20)), ("sy", 64),
+        ("rows", 4), ("cols", 64), ("layout", SPLIT), ("act", SILU), ("dtype", BF16),
+        ("ws", WS), ("wsb", 1 << 20), ("s1", None), ("s2", None), ("s3", None))])
+    assert fh(rows=0) == OK and fh(act=7) == ENUM and fh(rows=-1) == SHAPE
+    assert fh(a=None) == NULL and fh(sy=3) == STRIDE
+    assert fh(y=BASE + (1 << 20) + 2) == ALIAS
+    assert fh(ws=None) == -7                                  # GLU_ERR_WORKSPACE
+    need = glu.glu_host_workspace_bytes(1, 64, SPLIT, BF16, 0)
+    assert fh(wsb=need - 1) == -7
+    bh = glu.glu_bwd_host(BASE, 64, BASE + (1 << 20), 64, BASE + (2 << 20), 64, BASE + (3 << 20), 64,
+                          BASE + (4 << 20), 64, 4, 64, SPLIT, SILU, BF16, WS, 16, None, None, None)
+    assert bh == -7
+
+
+def test_host_workspace_size_formula():
+    ws = glu.glu_host_workspace_bytes
+    # two slots; each staged matrix rounded up to 256 bytes
+    assert ws(1, 64, SPLIT, BF16, 0) == 2 * 3 * 256
+    assert ws(100, 1000, SPLIT, BF16, 0) == 2 * 3 * (200192)                  # 100*1000*2 -> 200192
+    assert ws(100, 1000, CONCAT, F32, 0) == 2 * (800000 + 400128)             # x (2I) | y
+    assert ws(10, 1024, SPLIT, F16, 1) == 2 * 5 * 20480                       # dc, a, b | da, db
+    assert ws(10, 1024, CONCAT, F16, 1) == 2 * (20480 + 40960 + 40960)        # dc, x | dx
+    assert ws(0, 64, SPLIT, BF16, 0) == 0 and ws(4, 64, 9, BF16, 0) == 0
