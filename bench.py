@@ -178,6 +178,7 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     glu.lib()
+    glu.glu_set_tuning(path={"default": 0, "direct": 1, "bulk": 2}[args.path])
 
     d = glu_synth.metric_bf16()
     host = {k: torch.from_numpy(d[k].view(np.int16)).pin_memory() for k in ("a", "b", "dc")}
@@ -403,6 +404,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=3.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--path", default="default", choices=["default", "direct", "bulk"],
+                    help="load path of the kernels (library default, direct loads, or bulk copies "
+                         "staged in shared memory); for profiling and comparisons")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

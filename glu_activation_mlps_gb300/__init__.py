@@ -30,7 +30,7 @@ STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STR
 # Every symbol include/glu.h declares.
 EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
-           "glu_set_tuning", "glu_get_tuning")
+           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts")
 
 
 class GluError(RuntimeError):
@@ -46,13 +46,14 @@ class LaunchInfo(ctypes.Structure):
     _fields_ = [("launched", ctypes.c_int32), ("backward", ctypes.c_int32),
                 ("vec_bytes", ctypes.c_int32), ("unroll", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("flattened", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("flattened", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("vector_units", ctypes.c_int64), ("tail_elems", ctypes.c_int64)]
 
 
 class Tuning(ctypes.Structure):
     _fields_ = [("vec_bytes", ctypes.c_int32), ("unroll", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("dependent_launch", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("dependent_launch", ctypes.c_int32),
+                ("path", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -99,6 +100,8 @@ def lib() -> ctypes.CDLL:
             L.glu_set_tuning.restype = ci
             L.glu_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
             L.glu_get_tuning.restype = ci
+            L.glu_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
+            L.glu_wait_timeouts.restype = ci
             _lib = L
     return _lib
 
@@ -150,15 +153,23 @@ def glu_last_launch() -> dict:
     st = lib().glu_last_launch(ctypes.byref(info))
     if st:
         raise GluError(st, "glu_last_launch")
-    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_ if f != "reserved"}
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
 
 
 def glu_set_tuning(vec_bytes: int = 0, unroll: int = 0, ctas_per_sm: int = 0,
-                   dependent_launch: int = 0) -> None:
-    t = Tuning(vec_bytes, unroll, ctas_per_sm, dependent_launch)
+                   dependent_launch: int = 0, path: int = 0) -> None:
+    t = Tuning(vec_bytes, unroll, ctas_per_sm, dependent_launch, path)
     st = lib().glu_set_tuning(ctypes.byref(t))
     if st:
         raise GluError(st, "glu_set_tuning")
+
+
+def glu_wait_timeouts(reset: bool = False) -> int:
+    c = ctypes.c_uint(0)
+    st = lib().glu_wait_timeouts(ctypes.byref(c), int(reset))
+    if st:
+        raise GluError(st, "glu_wait_timeouts")
+    return c.value
 
 
 def glu_get_tuning() -> dict:
@@ -167,7 +178,7 @@ def glu_get_tuning() -> dict:
     if st:
         raise GluError(st, "glu_get_tuning")
     return {"vec_bytes": t.vec_bytes, "unroll": t.unroll, "ctas_per_sm": t.ctas_per_sm,
-            "dependent_launch": t.dependent_launch}
+            "dependent_launch": t.dependent_launch, "path": t.path}
 
 
 # ---- torch tensor marshalling -------------------------------------------------

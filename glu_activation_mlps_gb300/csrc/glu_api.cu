@@ -25,6 +25,7 @@ std::atomic<int32_t> g_vec_bytes{0};
 std::atomic<int32_t> g_unroll{0};
 std::atomic<int32_t> g_ctas_per_sm{0};
 std::atomic<int32_t> g_dependent_launch{0};
+std::atomic<int32_t> g_path{0};                // 0 default, 1 direct loads, 2 bulk copies
 constexpr int32_t kDefaultCtasPerSm = -1;     // one block per tile
 
 // Default access width (bytes) and accesses in flight per operand per thread,
@@ -135,7 +136,114 @@ using glu::cuda_fail;
 
 using glu::Call;
 
+// Launches `fn` with the programmatic-dependency attribute unless switched
+// off; falls back to an ordinary launch if the runtime refuses the attribute.
+cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, void **args,
+                          cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const bool dependent = g_dependent_launch.load(std::memory_order_relaxed) >= 0;
+    cfg.attrs = dependent ? attr : nullptr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess && dependent) {
+        (void)cudaGetLastError();
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelExC(&cfg, fn, args);
+    }
+    return e;
+}
+
+int plan_direct(const Call &c, cudaStream_t stream);
+
+// Bulk-copy staging path: contiguous operands, 16-byte aligned, at least one
+// whole chunk.  Whole chunks go to the bulk kernel (one block per SM), the
+// remainder to the direct kernel.  Returns 1 if the call is not eligible.
+int plan_bulk(const Call &c, cudaStream_t stream)
+{
+    const int n_ops = c.dir == kBwd ? 5 : 3;
+    const uintptr_t ptrs[5] = {uintptr_t(c.a), uintptr_t(c.b), uintptr_t(c.y0), uintptr_t(c.dc),
+                               uintptr_t(c.y1)};
+    const int64_t strides[5] = {c.sa, c.sb, c.sy0, c.sdc, c.sy1};
+    bool flat = true;
+    for (int i = 0; i < n_ops; ++i) {
+        flat = flat && (c.rows == 1 || strides[i] == c.cols);
+        flat = flat && (ptrs[i] % 16 == 0);
+    }
+    const int64_t bytes = c.rows * c.cols * c.E;
+    const int64_t chunks = bytes / glu::kBulkChunkHost;
+    if (!flat || chunks < 1) return 1;
+
+    // ctas_per_sm 1 selects the wide shape, anything else the narrow one
+    const bool narrow = g_ctas_per_sm.load(std::memory_order_relaxed) != 1;
+    static std::atomic<int> smem_set[3][4][2][2];
+    glu::BulkFn fn = glu::bulk_kernel(c.dtype, c.act, c.dir, narrow);
+    if (!fn) return GLU_ERR_ENUM;
+    const int smem = glu::bulk_smem_bytes(c.dir, narrow);
+    std::atomic<int> &flag = smem_set[c.dtype][c.act][c.dir][narrow];
+    if (!flag.load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) { (void)cudaGetLastError(); return cuda_fail(e); }
+        flag.store(1, std::memory_order_release);
+    }
+    const int sms = sm_count();
+    if (sms <= 0) return cuda_fail(cudaGetLastError());
+    glu::BulkParams bp{c.a, c.b, c.dc, c.y0, c.y1, chunks};
+    void *args[] = {&bp};
+    const int64_t slots = int64_t(sms) * (narrow ? 2 : 1);
+    const int64_t grid = chunks < slots ? chunks : slots;
+    const int threads = glu::bulk_threads(narrow);
+    cudaError_t e = launch_kernel(reinterpret_cast<const void *>(fn), dim3(unsigned(grid)),
+                                  dim3(threads), size_t(smem), args, stream);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return cuda_fail(e); }
+
+    glu_launch_info_t info{};
+    info.launched = 1;
+    info.backward = c.dir == kBwd;
+    info.vec_bytes = 16;
+    info.unroll = 1;
+    info.threads = threads;
+    info.grid = int32_t(grid);
+    info.flattened = c.rows > 1;
+    info.path = 2;
+    info.vector_units = chunks * (glu::kBulkChunkHost / 16);
+    const int64_t done_elems = chunks * glu::kBulkChunkHost / c.E;
+    const int64_t rest = c.rows * c.cols - done_elems;
+    info.tail_elems = rest;
+    if (rest > 0) {
+        Call r = c;
+        const int64_t off = done_elems * c.E;
+        r.rows = 1;
+        r.cols = rest;
+        r.a = c.a + off; r.b = c.b + off; r.y0 = c.y0 + off;
+        if (c.dir == kBwd) { r.dc = c.dc + off; r.y1 = c.y1 + off; }
+        r.sa = r.sb = r.sy0 = r.sdc = r.sy1 = rest;
+        const int st = plan_direct(r, stream);
+        if (st != GLU_OK) return st;
+    }
+    t_last_launch = info;
+    return GLU_OK;
+}
+
 int plan_and_launch(const Call &c, cudaStream_t stream)
+{
+    if (g_path.load(std::memory_order_relaxed) == 2) {
+        const int st = plan_bulk(c, stream);
+        if (st != 1) return st;
+    }
+    return plan_direct(c, stream);
+}
+
+int plan_direct(const Call &c, cudaStream_t stream)
 {
     const int E = c.E;
     const int n_ops = c.dir == glu::kBwd ? 5 : 3;
@@ -214,27 +322,10 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
     // Launch with a programmatic dependency on the previous kernel in the
     // stream (unless switched off): the kernel waits for that grid itself, so
     // ordering and visibility are unchanged, but its blocks can be scheduled
-    // during the previous grid's tail.  If the runtime refuses the attribute,
-    // fall back to an ordinary launch.
+    // during the previous grid's tail.
     void *args[] = {&p};
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(blocks));
-    cfg.blockDim = dim3(glu::kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    const bool dependent = g_dependent_launch.load(std::memory_order_relaxed) >= 0;
-    cfg.attrs = dependent ? attr : nullptr;
-    cfg.numAttrs = dependent ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
-    if (e != cudaSuccess && dependent) {
-        (void)cudaGetLastError();
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
-        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
-    }
+    cudaError_t e = launch_kernel(reinterpret_cast<const void *>(fn), dim3(unsigned(blocks)),
+                                  dim3(glu::kThreads), 0, args, stream);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return cuda_fail(e);
@@ -248,6 +339,7 @@ int plan_and_launch(const Call &c, cudaStream_t stream)
     info.threads = glu::kThreads;
     info.grid = int32_t(blocks);
     info.flattened = flat && c.rows > 1;
+    info.path = 1;
     info.vector_units = p.units;
     info.tail_elems = p.tail_units;
     t_last_launch = info;
@@ -412,6 +504,13 @@ const char *glu_last_cuda_error(void) { return t_cuda_error; }
 
 int glu_version(void) { return GLU_VERSION; }
 
+int glu_wait_timeouts(unsigned int *count, int reset)
+{
+    if (!count) return GLU_ERR_NULL;
+    cudaError_t e = glu::bulk_timeouts(count, reset != 0);
+    return e == cudaSuccess ? GLU_OK : cuda_fail(e);
+}
+
 int glu_last_launch(glu_launch_info_t *out)
 {
     if (!out) return GLU_ERR_NULL;
@@ -423,6 +522,8 @@ int glu_set_tuning(const glu_tuning_t *t)
 {
     if (!t) return GLU_ERR_NULL;
     const int32_t v = t->vec_bytes, u = t->unroll, c = t->ctas_per_sm, d = t->dependent_launch;
+    const int32_t path = t->path;
+    if (path < 0 || path > 2) return GLU_ERR_ENUM;
     if (!(v == 0 || v == 32 || v == 16 || v == 4 || v == 2)) return GLU_ERR_ENUM;
     if (!(u == 0 || u == 1 || u == 2 || u == 4)) return GLU_ERR_ENUM;
     if (c > 64) return GLU_ERR_ENUM;
@@ -431,6 +532,7 @@ int glu_set_tuning(const glu_tuning_t *t)
     g_unroll.store(u);
     g_ctas_per_sm.store(c);
     g_dependent_launch.store(d);
+    g_path.store(path);
     return GLU_OK;
 }
 
@@ -441,6 +543,7 @@ int glu_get_tuning(glu_tuning_t *out)
     out->unroll = g_unroll.load();
     out->ctas_per_sm = g_ctas_per_sm.load();
     out->dependent_launch = g_dependent_launch.load();
+    out->path = g_path.load();
     return GLU_OK;
 }
 

@@ -68,6 +68,21 @@ KernelFn kernel_bf16(int act, int dir, int vb_sel, int unroll_sel);
 
 constexpr int kThreads = 256;
 
+// Bulk-copy staging kernels (glu_bulk.cu): contiguous operands only, one
+// ("wide") or two ("narrow") blocks per SM, `chunks` chunks of kBulkChunkHost
+// bytes per operand.
+struct BulkParams {
+    const char *a, *b, *dc;        // inputs (dc: backward only)
+    char *y0, *y1;                 // outputs (y1: backward only)
+    int64_t chunks;                // whole chunks of kBulkChunkHost bytes per operand
+};
+using BulkFn = void (*)(BulkParams);
+constexpr int kBulkChunkHost = 16384;
+BulkFn bulk_kernel(int dtype, int act, int dir, bool narrow);
+int bulk_smem_bytes(int dir, bool narrow);
+int bulk_threads(bool narrow);
+cudaError_t bulk_timeouts(unsigned int *count, bool reset);
+
 // One validated call: what the planner needs.  Strides are in elements.
 struct Call {
     int dir, act, dtype, E;

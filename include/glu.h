@@ -212,7 +212,7 @@ typedef struct {
     int32_t threads;      /* threads per block */
     int32_t grid;         /* blocks launched */
     int32_t flattened;    /* 1 if the rows were contiguous and walked as one row */
-    int32_t reserved;
+    int32_t path;         /* 1 = direct loads, 2 = bulk copies staged in shared memory */
     int64_t vector_units; /* full-width accesses per operand */
     int64_t tail_elems;   /* elements handled one at a time (row ends) */
 } glu_launch_info_t;
@@ -232,16 +232,28 @@ int glu_last_launch(glu_launch_info_t *out);
  *                 0 or 1: launch with a programmatic dependency on the previous
  *                 kernel in the stream (the kernel still waits for that grid to
  *                 finish before touching memory, so results and ordering are
- *                 unchanged; only scheduling overlaps); -1: ordinary launch */
+ *                 unchanged; only scheduling overlaps); -1: ordinary launch
+ *   path          0 or 1: direct 16/32-byte loads into registers; 2: for
+ *                 contiguous, 16-byte aligned operands, whole 16 KiB chunks are
+ *                 staged in shared memory by the bulk-copy engine (one block
+ *                 per SM) and the rest takes the direct path */
 typedef struct {
     int32_t vec_bytes;
     int32_t unroll;
     int32_t ctas_per_sm;
     int32_t dependent_launch;
+    int32_t path;
 } glu_tuning_t;
 
 int glu_set_tuning(const glu_tuning_t *t);   /* GLU_ERR_ENUM for unsupported values */
 int glu_get_tuning(glu_tuning_t *out);
+
+/* Kernels that wait on the bulk-copy engine bound every wait (about a second)
+ * and count the waits that ran out on the current device instead of hanging.
+ * Copies that count into *count (synchronising with the device) and, if
+ * `reset`, sets it back to 0.  A nonzero count means some outputs of those
+ * launches were not written. */
+int glu_wait_timeouts(unsigned int *count, int reset);
 
 #ifdef __cplusplus
 }

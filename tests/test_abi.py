@@ -136,13 +136,15 @@ def test_valid_calls_reach_the_cuda_runtime_without_a_gpu():
 
 
 def test_tuning_roundtrip_and_validation():
-    glu.glu_set_tuning(16, 4, 8, -1)
-    assert glu.glu_get_tuning() == {"vec_bytes": 16, "unroll": 4, "ctas_per_sm": 8, "dependent_launch": -1}
-    for bad in ((8, 0, 0, 0), (0, 3, 0, 0), (0, 0, 100, 0), (0, 0, 0, 2)):
+    glu.glu_set_tuning(16, 4, 8, -1, 2)
+    assert glu.glu_get_tuning() == {"vec_bytes": 16, "unroll": 4, "ctas_per_sm": 8, "dependent_launch": -1,
+                                    "path": 2}
+    for bad in ((8, 0, 0, 0, 0), (0, 3, 0, 0, 0), (0, 0, 100, 0, 0), (0, 0, 0, 2, 0), (0, 0, 0, 0, 3)):
         with pytest.raises(glu.GluError):
             glu.glu_set_tuning(*bad)
-    glu.glu_set_tuning(0, 0, 0, 0)
-    assert glu.glu_get_tuning() == {"vec_bytes": 0, "unroll": 0, "ctas_per_sm": 0, "dependent_launch": 0}
+    glu.glu_set_tuning(0, 0, 0, 0, 0)
+    assert glu.glu_get_tuning() == {"vec_bytes": 0, "unroll": 0, "ctas_per_sm": 0, "dependent_launch": 0,
+                                    "path": 0}
 
 
 def test_last_launch_requires_pointer():
