@@ -28,7 +28,8 @@ STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STR
           -4: "GLU_ERR_ALIAS", -5: "GLU_ERR_ENUM", -6: "GLU_ERR_CUDA", -7: "GLU_ERR_WORKSPACE"}
 
 # Every symbol include/glu.h declares.
-EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_host_workspace_bytes",
+EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_fwd_host_noalloc",
+           "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
            "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts")
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
             L.glu_bwd_host.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci,
                                        vp, sz, vp, vp, vp]
             L.glu_bwd_host.restype = ci
+            L.glu_fwd_host_noalloc.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, ci, ci, ci, vp]
+            L.glu_fwd_host_noalloc.restype = ci
             L.glu_host_workspace_bytes.argtypes = [i64, i64, ci, ci, ci]
             L.glu_host_workspace_bytes.restype = sz
             L.glu_status_string.argtypes = [ci]
@@ -130,6 +133,14 @@ def glu_bwd_host(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_
     return lib().glu_bwd_host(dc, dc_stride, a, a_stride, b, b_stride, da, da_stride, db, db_stride,
                               n_rows, n_cols, layout, act, dtype, workspace, workspace_bytes,
                               copy_in, compute, copy_out)
+
+
+def glu_fwd_host_noalloc(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols, layout, act, dtype,
+                         stream) -> int:
+    """glu_fwd_host staged through the library's own fixed device array: for
+    callers that cannot allocate device memory (see include/glu.h)."""
+    return lib().glu_fwd_host_noalloc(a, a_stride, b, b_stride, y, y_stride, n_rows, n_cols, layout,
+                                      act, dtype, stream)
 
 
 def glu_host_workspace_bytes(rows_per_block, n_cols, layout, dtype, backward) -> int:

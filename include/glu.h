@@ -186,6 +186,36 @@ int glu_bwd_host(const void *dc, int64_t dc_stride,
                  void *workspace, size_t workspace_bytes,
                  glu_stream_t copy_in, glu_stream_t compute, glu_stream_t copy_out);
 
+/*
+ * glu_fwd_host without a caller workspace, for callers that cannot allocate
+ * device memory at all: a plug-in inside an application whose own allocator
+ * owns the device memory and gives none out, or a process that fixes its
+ * memory budget at start-up and must not allocate while running.  The source
+ * pages have no counterpart to this entry point; it is a deployment aid.
+ *
+ * Same arguments and rules as glu_fwd_host minus the workspace; one stream
+ * carries the copies and the kernels, in order.  Blocks of rows are staged in
+ * a fixed device array of GLU_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits.  Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no event or stream creation.
+ *   - A row that does not fit the array (inputs and output of one row, for
+ *     SPLIT 3 * n_cols elements, for CONCAT 3 * n_cols) is rejected with
+ *     GLU_ERR_WORKSPACE.
+ *   - The first call on each device looks up the array's device address (a
+ *     CUDA runtime query); make that first call before any stream capture.
+ *   - Every call uses the same array, which keeps the last call's contents
+ *     (no part of it needs to start at zero): calls whose work can overlap on
+ *     the GPU race on it, so order them, e.g. on one stream.
+ */
+#define GLU_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int glu_fwd_host_noalloc(const void *a, int64_t a_stride,
+                         const void *b, int64_t b_stride,
+                         void *y, int64_t y_stride,
+                         int64_t n_rows, int64_t n_cols,
+                         glu_layout_t layout, glu_act_t act, glu_dtype_t dtype,
+                         glu_stream_t stream);
+
 /* Workspace bytes glu_fwd_host (backward == 0) or glu_bwd_host (backward != 0)
  * needs for blocks of `rows_per_block` rows of `n_cols` columns; 0 for invalid
  * arguments. */
