@@ -334,6 +334,101 @@ def run_gpu(args, rank, world, local_rank):
     return line
 
 
+# ---------------------------------------------------------------- throughput table
+
+def run_table(args):
+    """Throughput of every named workload with the library defaults (or the
+    --path given): back-to-back launches over rotating sets of buffers whose
+    total exceeds L2, median of rounds, against the measured copy bandwidth.
+    Prints a markdown table (not the benchmark's JSON line)."""
+    import torch
+    import glu_activation_mlps_gb300 as glu
+
+    glu.build()
+    L = glu.lib()
+    glu.glu_set_tuning(path={"default": 0, "direct": 1, "bulk": 2}[args.path])
+    peak, src = measured_peak()
+    s = torch.cuda.current_stream().cuda_stream
+    TD = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+    EB = {"bf16": 2, "f16": 2, "f32": 4}
+    code = {"bf16": 2, "f16": 1, "f32": 0}
+    gen = torch.Generator(device="cuda").manual_seed(0)
+
+    def sets_for(nbytes_per_set, make):
+        n = max(2, -(-600 * 2**20 // nbytes_per_set))
+        return [make() for _ in range(n)]
+
+    def timed(fn, nsets, reps=40, rounds=5):
+        out = []
+        for _ in range(rounds):
+            for k in range(5):
+                fn(k % nsets)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for k in range(reps):
+                fn(k % nsets)
+            e1.record()
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) / reps * 1e3)
+        return statistics.median(out)
+
+    rows = []
+
+    def split_case(name, R, C, dt, act, direction, sigma=1.0):
+        E_ = EB[dt]
+
+        def make():
+            t = [(torch.randn(R, C, device="cuda", generator=gen) * sigma).to(TD[dt]) for _ in range(3)]
+            return t + [torch.empty_like(t[0]) for _ in range(2)]
+        sets = sets_for(5 * R * C * E_, make)
+        a_ = glu.ACT[act]
+
+        def fn(k):
+            A, B, DC, Y0, Y1 = sets[k]
+            if direction == "fwd":
+                st = L.glu_fwd(A.data_ptr(), C, B.data_ptr(), C, Y0.data_ptr(), C, R, C, 0, a_, code[dt], s)
+            else:
+                st = L.glu_bwd(DC.data_ptr(), C, A.data_ptr(), C, B.data_ptr(), C, Y0.data_ptr(), C,
+                               Y1.data_ptr(), C, R, C, 0, a_, code[dt], s)
+            assert st == 0
+        us = timed(fn, len(sets))
+        nb = (3 if direction == "fwd" else 5) * E_ * R * C
+        rows.append((name, f"{R}x{C}", dt, act, direction, us, nb / us / 1e3))
+
+    def concat_case(name, R, C, inplace):
+        def make():
+            x = (torch.randn(R, 2 * C, device="cuda", generator=gen) * 1.5).to(torch.bfloat16)
+            return [x, torch.empty(R, C, dtype=torch.bfloat16, device="cuda")]
+        sets = sets_for(3 * R * C * 2, make)
+
+        def fn(k):
+            X, Y = sets[k]
+            y, ys = (X[:, C:], 2 * C) if inplace else (Y, C)
+            st = L.glu_fwd(X.data_ptr(), 2 * C, None, 0, y.data_ptr(), ys, R, C, 1, 0, 2, s)
+            assert st == 0
+        us = timed(fn, len(sets))
+        rows.append((name, f"{R}x(2x{C})", "bf16", "silu", "fwd", us, 6 * R * C / us / 1e3))
+
+    split_case("fwd f32 small", 256, 1024, "f32", "silu", "fwd")
+    split_case("fwd bf16", 4096, 11008, "bf16", "silu", "fwd", sigma=2.0)
+    concat_case("fwd bf16 [gate|up]", 4096, 18944, False)
+    concat_case("fwd bf16 [gate|up] in place", 4096, 18944, True)
+    split_case("bwd bf16 (in-place shape)", 4096, 28672, "bf16", "silu", "bwd", sigma=3.0)
+    split_case("metric fwd", ROWS, COLS, "bf16", "silu", "fwd")
+    split_case("metric bwd", ROWS, COLS, "bf16", "silu", "bwd")
+    for dt in glu_synth.SWEEP_DTYPES:
+        for H in glu_synth.SWEEP_H:
+            for act in glu_synth.SWEEP_ACTS:
+                for d in ("fwd", "bwd"):
+                    split_case("sweep", 4096, H, dt, act, d)
+    print(f"| workload | shape | dtype | act | dir | us / launch | GB/s | % of {peak:.0f} GB/s ({src}) |")
+    print("|---|---|---|---|---|---|---|---|")
+    for name, shape, dt, act, d, us, gbs in rows:
+        print(f"| {name} | {shape} | {dt} | {act} | {d} | {us:.2f} | {gbs:.0f} | {100 * gbs / peak:.1f} |",
+              flush=True)
+
+
 # ---------------------------------------------------------------- CPU oracle arms
 
 def oracle_rows(orc, d, r0, r1, threads):
@@ -404,6 +499,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=3.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--table", action="store_true",
+                    help="print a throughput table of every named workload instead of the JSON line")
     ap.add_argument("--path", default="default", choices=["default", "direct", "bulk"],
                     help="load path of the kernels (library default, direct loads, or bulk copies "
                          "staged in shared memory); for profiling and comparisons")
@@ -414,6 +511,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.table:
+        run_table(args)
+        return
 
     if args.impl == "reference":
         if rank == 0:
