@@ -1,12 +1,12 @@
-"""Generates the lower-tail normal-CDF approximation used by the GeGLU-erf
-kernels for bf16 / f16 storage (the constants of `phi_tail_poly` in
-glu_math.cuh).
+"""Generates the lower-tail normal-CDF approximations used by the GeGLU-erf
+kernels (the coefficient tables of `phi_tail` in glu_math.cuh): degree 7 for
+bf16 / f16 storage, degree 10 for f32 storage.
 
 For x >= 0 the lower tail of the standard normal distribution is written as
 
     Phi(-x) = 0.5 * erfc(x / sqrt 2) = exp(-x^2 / 2) * t * P(t),   t = 1 / (1 + C x),
 
-with P a polynomial of degree DEG on t in (0, 1].  P is smooth there: at t = 1
+with P a polynomial of degree DEG on t in (0, 1] (both fits use C = 0.3).  P is smooth there: at t = 1
 (x = 0) it is 1/2, and as t -> 0 (x -> infinity) it tends to C / sqrt(2 pi),
 because Phi(-x) ~ exp(-x^2/2) / (x sqrt(2 pi)) (Mills' ratio).  The exact P is
 evaluated with mpmath; the coefficients minimise the maximum relative error
@@ -62,10 +62,11 @@ def check(coef32):
 
 
 if __name__ == "__main__":
-    coef = fit()
-    e64, e32 = check(coef)
-    print(f"// Phi(-x) = exp(-x^2/2) * t * P(t), t = 1/(1 + {C} x), degree {DEG}")
-    print(f"// max relative error of P: {e64:.2e} (float32 coefficients), {e32:.2e} (float32 Horner)")
-    print(f"constexpr float kPhiTailC = {C}f;")
-    print("constexpr float kPhiTailP[%d] = {" % (DEG + 1))
-    print(",\n".join(f"    {float(v):.9e}f" for v in coef) + "};")
+    print(f"// Phi(-x) = exp(-x^2/2) * t * P(t), t = 1/(1 + {C} x)")
+    for deg, use in ((7, "bf16 / f16 storage"), (10, "f32 storage")):
+        DEG = deg
+        coef = fit()
+        e64, e32 = check(coef)
+        print(f"// degree {DEG} ({use}): max relative error of P {e64:.2e} with float32 "
+              f"coefficients, {e32:.2e} with float32 Horner")
+        print("{" + ", ".join(f"{float(v):.9e}f" for v in coef) + "}")

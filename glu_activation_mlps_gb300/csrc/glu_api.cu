@@ -275,7 +275,12 @@ int plan_direct(const Call &c, cudaStream_t stream)
         if (ok) { vb = cand; break; }
     }
     int32_t unroll = g_unroll.load(std::memory_order_relaxed);
-    if (unroll == 0) unroll = dflt.unroll;
+    if (unroll == 0) {
+        // Matrices of up to 2^22 elements fill only one or two waves of
+        // blocks; one access in flight per thread doubles the blocks and
+        // evens out the last wave.
+        unroll = c.rows * c.cols <= (int64_t(1) << 22) ? 1 : dflt.unroll;
+    }
     const int unroll_sel = unroll == 1 ? 0 : (unroll == 2 ? 1 : 2);
     const int vb_sel = vb == 32 ? 0 : (vb == 16 ? 1 : 2);
     if (vb == 0) unroll = 1;

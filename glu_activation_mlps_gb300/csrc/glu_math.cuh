@@ -15,7 +15,8 @@
 //                       = e (1 + x + e) / (1+e)^2            for x < 0
 //                         (the only cancellation left is (1 + x) + e near the
 //                         root x* = -1.2785, where 1 + x is exact in fp32)
-//   1 + erf(z)          = erfc(-z)              (no cancellation for z < 0)
+//   0.5 (1 + erf(x/sqrt2)) = Phi(x) = 1 - Phi(-x), with the lower tail Phi(-|x|)
+//                         computed directly (no cancellation for x < 0)
 //   0.5 (1 + tanh(u))   = sigmoid(2u)           (no cancellation for u < 0)
 //
 // Near the root x* of act' (silu' at -1.2785, both GELU' near -0.752) the two
@@ -27,7 +28,7 @@
 // coefficients are act^(k+1)(x*)/k!, from the closed forms above.
 //
 // `Exact` selects the variant used when the storage dtype is fp32: there the
-// rounding of the scaled arguments (x/sqrt2, the tanh polynomial, x^2) would be
+// rounding of the scaled arguments (the tanh polynomial, x^2) would be
 // amplified by up to 2z^2 in the tails, so those arguments are carried as
 // (hi, lo) float pairs and the first-order effect of `lo` is applied
 // analytically.  For fp16/bf16 outputs the plain fp32 forms are far below
@@ -82,9 +83,6 @@ __device__ __forceinline__ SigmoidParts sigmoid_parts(float x)
 
 // (hi, lo) splits of constants: hi is the nearest float, lo the nearest float
 // to the remainder.
-constexpr float kInvSqrt2Hi = 0.707106769f;         // 1/sqrt(2)
-constexpr float kInvSqrt2Lo = 1.21016175e-08f;
-constexpr float kTwoOverSqrtPi = 1.12837923f;       // 2/sqrt(pi) = -d/dz erfc(z) at 0
 constexpr float kInvSqrt2Pi = 0.398942292f;         // 1/sqrt(2 pi)
 // tanh form: w(x) = 2u(x) = C1 x + C3 x^3 with C1 = 2 sqrt(2/pi), C3 = C1 * 0.044715
 constexpr float kC1Hi = 1.59576917f;
@@ -121,19 +119,26 @@ __device__ __forceinline__ void root_series(float x, const RootSeries r, float *
     if (fabsf(u) < kRootRadius) *dact = u * fmaf(u, fmaf(u, fmaf(u, r.c4, r.c3), r.c2), r.c1);
 }
 
-// Lower tail of the standard normal for bf16/f16 storage:
+// Lower tail of the standard normal:
 //     Phi(-x) = exp(-x^2/2) * t * P(t),  t = 1/(1 + 0.3 x),  x >= 0,
-// with P of degree 7 fitted to the exact ratio (Mills' ratio form; relative
-// error of P <= 2.7e-6 in float32).  The coefficients are produced by
+// with P a polynomial fitted to the exact ratio (Mills' ratio form): degree 7
+// for bf16/f16 storage (relative error of P <= 2.7e-6 in float32), degree 10
+// for f32 storage (<= 1.4e-7).  The coefficients are produced by
 // gen_phi_tail.py next to this file.  The exponential is returned too: it is
-// also sqrt(2 pi) phi(x), the density the GeGLU-erf backward needs.
+// also sqrt(2 pi) phi(x), the density the GeGLU-erf backward needs.  For f32
+// storage, x^2 is carried as p + pe (exact) and exp(-x^2/2) =
+// exp(-p/2) (1 - pe/2), and 1/(1 + 0.3 x) is rounded correctly.
 constexpr float kPhiTailC = 0.3f;
-__host__ __device__ constexpr float phi_tail_coef(int i)
+__host__ __device__ constexpr float phi_tail_coef(bool exact, int i)
 {
-    constexpr float p[8] = {1.196823716e-01f, 1.197295263e-01f, 1.077751145e-01f,
-                            9.759789705e-02f, 1.416620519e-02f, 1.230392978e-01f,
-                            -1.036966890e-01f, 2.170499042e-02f};
-    return p[i];
+    constexpr float p7[8] = {1.196823716e-01f, 1.197295263e-01f, 1.077751145e-01f,
+                             9.759789705e-02f, 1.416620519e-02f, 1.230392978e-01f,
+                             -1.036966890e-01f, 2.170499042e-02f};
+    constexpr float p10[11] = {1.196826845e-01f, 1.196820512e-01f, 1.089364216e-01f,
+                               8.699049801e-02f, 6.073883548e-02f, 1.550978515e-02f,
+                               2.356493101e-02f, -3.294012696e-02f, -3.021260537e-02f,
+                               3.880830109e-02f, -1.076079253e-02f};
+    return exact ? p10[i] : p7[i];
 }
 
 struct PhiTail {
@@ -141,33 +146,26 @@ struct PhiTail {
     float e;   // exp(-x^2 / 2)
 };
 
+template <bool Exact>
 __device__ __forceinline__ PhiTail phi_tail(float x)   // x = |a| >= 0
 {
     PhiTail r;
-    r.e = exp_neg<false>(0.5f * x * x);
     float t;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(kPhiTailC, x, 1.0f)));   // t in (0, 1]
-    float p = phi_tail_coef(7);
-#pragma unroll
-    for (int i = 6; i >= 0; --i) p = fmaf(p, t, phi_tail_coef(i));
-    r.q = r.e * (t * p);
-    return r;
-}
-
-// erfc(-x / sqrt 2), the 2 Phi(x) of the GeGLU erf form.
-template <bool Exact>
-__device__ __forceinline__ float two_phi(float x)
-{
-    float zh = __fmul_rn(-x, kInvSqrt2Hi);
-    float v = erfcf(zh);
     if (Exact) {
-        // z = zh + zl exactly up to the lo constant; erfc(zh + zl) =
-        // erfc(zh) - (2/sqrt pi) exp(-zh^2) zl to first order.
-        float zl = fmaf(-x, kInvSqrt2Hi, -zh) + (-x) * kInvSqrt2Lo;
-        float g = expf(-zh * zh);            // 0 (not NaN) once zh^2 overflows
-        v = fmaf(-kTwoOverSqrtPi * g, zl, v);
+        const float xc = fminf(x, 40.0f);                  // Phi(-40) is 0 in fp32
+        const float p = __fmul_rn(xc, xc);
+        r.e = expf(-0.5f * p) * (1.0f - 0.5f * fmaf(xc, xc, -p));
+        t = __frcp_rn(fmaf(kPhiTailC, x, 1.0f));
+    } else {
+        r.e = exp_neg<false>(0.5f * x * x);
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(kPhiTailC, x, 1.0f)));   // t in (0, 1]
     }
-    return v;
+    constexpr int kDeg = Exact ? 10 : 7;
+    float poly = phi_tail_coef(Exact, kDeg);
+#pragma unroll
+    for (int i = kDeg - 1; i >= 0; --i) poly = fmaf(poly, t, phi_tail_coef(Exact, i));
+    r.q = r.e * (t * poly);
+    return r;
 }
 
 // w(x) = 2 sqrt(2/pi) (x + 0.044715 x^3) as hi (+ lo when Exact).
@@ -220,31 +218,16 @@ struct GeluErf {
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
-        if (!Exact) {
-            const float q = phi_tail(fabsf(x)).q;          // Phi(-|x|)
-            return x * (x <= 0.0f ? q : 1.0f - q);          // x Phi(x)
-        }
-        return 0.5f * x * two_phi<Exact>(x);
+        const float q = phi_tail<Exact>(fabsf(x)).q;       // Phi(-|x|)
+        return x * (x <= 0.0f ? q : 1.0f - q);              // x Phi(x)
     }
     template <bool Exact>
     __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
     {
-        if (!Exact) {
-            const PhiTail t = phi_tail(fabsf(x));
-            const float cdf = x <= 0.0f ? t.q : 1.0f - t.q;  // Phi(x)
-            *act = x * cdf;
-            *dact = fmaf(x, kInvSqrt2Pi * t.e, cdf);        // Phi + x phi
-            root_series(x, gelu_erf_root(), dact);
-            return;
-        }
-        float phi2 = two_phi<Exact>(x);                     // 2 Phi(x)
-        float ax = fminf(fabsf(x), 40.0f);                  // phi(40) is 0 in fp32
-        float p = __fmul_rn(ax, ax);
-        float g = exp_neg<Exact>(0.5f * p);
-        if (Exact) g = g * (1.0f - 0.5f * fmaf(ax, ax, -p));  // x^2 = p + pe
-        float pdf = kInvSqrt2Pi * g;                        // phi(x)
-        *act = 0.5f * x * phi2;
-        *dact = fmaf(x, pdf, 0.5f * phi2);                  // Phi + x phi
+        const PhiTail t = phi_tail<Exact>(fabsf(x));
+        const float cdf = x <= 0.0f ? t.q : 1.0f - t.q;     // Phi(x)
+        *act = x * cdf;
+        *dact = fmaf(x, kInvSqrt2Pi * t.e, cdf);            // Phi + x phi
         root_series(x, gelu_erf_root(), dact);
     }
 };
