@@ -89,6 +89,27 @@ def ncu_traffic():
     return t.get("bwd_dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- ranks
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of `x` over all ranks (the job's time is its slowest rank's); the
+    value itself when no process group is running.  Only timings travel: the
+    ranks exchange no data of the computation."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own batch (weak scaling), so
+    the job moves world * steps * bytes_per_step in the slowest rank's time."""
+    return world * steps * bytes_per_step / (ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -251,10 +272,7 @@ def run_gpu(args, rank, world, local_rank):
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(total_ms, dev)
 
     # end to end through the C ABI's host-memory entry points: a, b, dc live in
     # page-locked host memory; each step's glu_fwd_host copies a, b in and y
@@ -289,11 +307,7 @@ def run_gpu(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)          # the compute stream waits for each call's last copy out
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dev)
     barrier()
 
     if rank != 0:
@@ -304,7 +318,7 @@ def run_gpu(args, rank, world, local_rank):
     fwd_avg = statistics.fmean(fwd_ms)
     achieved = BWD_BYTES / (bwd_avg * 1e-3) / 1e9
     traffic = ncu_traffic()
-    value = world * K * STEP_BYTES / (total_ms * 1e-3) / 1e9
+    value = job_gbs(world, K, STEP_BYTES, total_ms)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
@@ -320,7 +334,7 @@ def run_gpu(args, rank, world, local_rank):
                        "bwd_gbs": round(achieved, 1),
                        "fwd_frac": round(FWD_BYTES / (fwd_avg * 1e-3) / 1e9 / peak, 4),
                        "fwd_min_ms": round(min(fwd_ms), 5), "bwd_min_ms": round(min(bwd_ms), 5)},
-        "e2e": {"value": round(world * Ke * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+        "e2e": {"value": round(job_gbs(world, Ke, STEP_BYTES, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": 5 * E * N_ELEMS, "d2h_bytes_per_step": 3 * E * N_ELEMS,
                 "steps": Ke, "ms_per_step": round(e2e_ms / Ke, 4),
                 "api": "glu_fwd_host + glu_bwd_host (pinned host buffers, 128 MiB device workspace)"},
