@@ -189,6 +189,33 @@ __device__ __forceinline__ void op_bwd(float c, float a, float b, float &da, flo
     db = c * s;                                                // dc * act(a)
 }
 
+// One storage word of the backward (1 or 2 elements): act and act' for every
+// element, the root series only on the rare path where an element lies next
+// to a root of act', then da = dc act' b and db = dc act.
+template <class Act, bool Exact, class Cd, int PW = Cd::kPerWord>
+__device__ __forceinline__ void bwd_word(uint32_t wa, uint32_t wb, uint32_t wc, float (&da)[PW],
+                                         float (&db)[PW])
+{
+    float a[PW], s[PW], ds[PW];
+    bool near = false;
+#pragma unroll
+    for (int e = 0; e < PW; ++e) {
+        a[e] = Cd::get(wa, e);
+        Act::template bwd_main<Exact>(a[e], &s[e], &ds[e]);
+        near |= Act::near_root(a[e]);
+    }
+    if (near) {
+#pragma unroll
+        for (int e = 0; e < PW; ++e) Act::fix_root(a[e], &ds[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < PW; ++e) {
+        const float c = Cd::get(wc, e), b = Cd::get(wb, e);
+        da[e] = c * ds[e] * b;                                 // dc * act'(a) * b
+        db[e] = c * s[e];                                      // dc * act(a)
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 // DIR = kFwd: (a, b) -> y0.   DIR = kBwd: (dc, a, b) -> (y0 = da, y1 = db).
 // VB = 32 or 16: vector units then the scalar tail; VB = 0: scalar tail only.
@@ -232,14 +259,12 @@ __global__ void __launch_bounds__(kThreads) glu_kernel(const Params p)
 #pragma unroll
                     for (int j = 0; j < W; ++j) {
                         float f0[PW], f1[PW];
+                        if constexpr (DIR == kFwd) {
 #pragma unroll
-                        for (int e = 0; e < PW; ++e) {
-                            const float a = C::get(va[k][j], e), b = C::get(vb[k][j], e);
-                            if constexpr (DIR == kFwd) {
-                                f0[e] = op_fwd<Act, kExact>(a, b);
-                            } else {
-                                op_bwd<Act, kExact>(C::get(vc[k][j], e), a, b, f0[e], f1[e]);
-                            }
+                            for (int e = 0; e < PW; ++e)
+                                f0[e] = op_fwd<Act, kExact>(C::get(va[k][j], e), C::get(vb[k][j], e));
+                        } else {
+                            bwd_word<Act, kExact, C>(va[k][j], vb[k][j], vc[k][j], f0, f1);
                         }
                         o0[j] = C::put(f0);
                         if constexpr (DIR == kBwd) o1[j] = C::put(f1);

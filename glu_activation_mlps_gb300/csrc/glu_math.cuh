@@ -119,6 +119,14 @@ __device__ __forceinline__ void root_series(float x, const RootSeries r, float *
     if (fabsf(u) < kRootRadius) *dact = u * fmaf(u, fmaf(u, fmaf(u, r.c4, r.c3), r.c2), r.c1);
 }
 
+// The cheap test the kernels run on every element; the series itself
+// (root_series) is only evaluated for the rare elements that pass it.  The
+// test is slightly wider than kRootRadius, so it never misses one.
+__device__ __forceinline__ bool near_root(float x, const RootSeries r)
+{
+    return fabsf(x - r.hi) < 1.0625f * kRootRadius;
+}
+
 // Lower tail of the standard normal:
 //     Phi(-x) = exp(-x^2/2) * t * P(t),  t = 1/(1 + 0.3 x),  x >= 0,
 // with P a polynomial fitted to the exact ratio (Mills' ratio form): degree 7
@@ -202,15 +210,31 @@ struct Silu {
         SigmoidParts p = sigmoid_parts<Exact>(x);
         return x * p.s;
     }
+    // act and act' without the root series (see bwd)
     template <bool Exact>
-    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
         SigmoidParts p = sigmoid_parts<Exact>(x);
         *act = x * p.s;
-        float num = x >= 0.0f ? fmaf(x, p.e, 1.0f + p.e)      // 1 + e + x e
-                              : p.e * ((1.0f + x) + p.e);     // e (1 + x + e)
+        float num;
+        if (Exact) {
+            num = x >= 0.0f ? fmaf(x, p.e, 1.0f + p.e)          // 1 + e + x e
+                            : p.e * ((1.0f + x) + p.e);         // e (1 + x + e)
+        } else {
+            // the same numerator as (1+e) m + x e, m = 1 (x >= 0) or e (x < 0):
+            // one FMA; its cancellation near the root is left to the series
+            const float d = 1.0f + p.e;
+            num = fmaf(x, p.e, d * (x >= 0.0f ? 1.0f : p.e));
+        }
         *dact = num * (p.r * p.r);
-        root_series(x, silu_root(), dact);
+    }
+    __device__ __forceinline__ static bool near_root(float x) { return glu::near_root(x, silu_root()); }
+    __device__ __forceinline__ static void fix_root(float x, float *dact) { root_series(x, silu_root(), dact); }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        bwd_main<Exact>(x, act, dact);
+        fix_root(x, dact);
     }
 };
 
@@ -222,13 +246,20 @@ struct GeluErf {
         return x * (x <= 0.0f ? q : 1.0f - q);              // x Phi(x)
     }
     template <bool Exact>
-    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
         const PhiTail t = phi_tail<Exact>(fabsf(x));
         const float cdf = x <= 0.0f ? t.q : 1.0f - t.q;     // Phi(x)
         *act = x * cdf;
         *dact = fmaf(x, kInvSqrt2Pi * t.e, cdf);            // Phi + x phi
-        root_series(x, gelu_erf_root(), dact);
+    }
+    __device__ __forceinline__ static bool near_root(float x) { return glu::near_root(x, gelu_erf_root()); }
+    __device__ __forceinline__ static void fix_root(float x, float *dact) { root_series(x, gelu_erf_root(), dact); }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        bwd_main<Exact>(x, act, dact);
+        fix_root(x, dact);
     }
 };
 
@@ -243,8 +274,16 @@ struct GeluTanh {
         if (Exact) s = fmaf(s * p.sm, lo, s);              // sigmoid(w + lo)
         return x * s;
     }
+    __device__ __forceinline__ static bool near_root(float x) { return glu::near_root(x, gelu_tanh_root()); }
+    __device__ __forceinline__ static void fix_root(float x, float *dact) { root_series(x, gelu_tanh_root(), dact); }
     template <bool Exact>
     __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        bwd_main<Exact>(x, act, dact);
+        fix_root(x, dact);
+    }
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
         float lo;
         float w = tanh_arg<Exact>(x, &lo);
@@ -258,7 +297,6 @@ struct GeluTanh {
         *act = x * s;
         // d/dx [x sigmoid(w)] = sigmoid(w) (1 + x (1 - sigmoid(w)) w')
         *dact = s * fmaf(xc * p.sm, dw, 1.0f);
-        root_series(x, gelu_tanh_root(), dact);
     }
 };
 
@@ -269,10 +307,17 @@ struct Relu {
         return x > 0.0f ? x : (x != x ? x : 0.0f);          // NaN propagates
     }
     template <bool Exact>
-    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
         *act = x > 0.0f ? x : (x != x ? x : 0.0f);
         *dact = x > 0.0f ? 1.0f : (x != x ? x : 0.0f);      // 0 at x == 0
+    }
+    __device__ __forceinline__ static bool near_root(float) { return false; }   // act' has no root
+    __device__ __forceinline__ static void fix_root(float, float *) {}
+    template <bool Exact>
+    __device__ __forceinline__ static void bwd(float x, float *act, float *dact)
+    {
+        bwd_main<Exact>(x, act, dact);
     }
 };
 
