@@ -1,0 +1,121 @@
+"""PyTorch autograd functions and modules over the C ABI.
+
+The pattern follows "Kernel Profile: SwiGLU (Tier 1 - Element-wise)" (Forward
+Pass, Backward Pass, Key Patterns): the forward saves the gate and up
+projections a and b and nothing else; the backward recomputes the activation
+from a in the kernel, and may write da over a and db over b (the saved tensors)
+instead of allocating.  Every computation runs in the library's CUDA kernels;
+these classes only marshal tensors.  "Skill: Write a Triton SiLU-Mul (SwiGLU)
+Kernel" (Purpose) gives the surrounding MLP, down(act(gate(x)) * up(x)).
+"""
+from __future__ import annotations
+
+import torch
+from torch import nn
+
+from . import bwd as _bwd
+from . import fwd as _fwd
+
+ACTS = ("silu", "gelu_erf", "gelu_tanh", "relu")
+
+
+def _check_act(act: str) -> str:
+    if act not in ACTS:
+        raise ValueError(f"unknown activation {act!r}; expected one of {ACTS}")
+    return act
+
+
+class GLUFunction(torch.autograd.Function):
+    """y = act(a) * b for separate gate and up tensors of one shape.
+
+    With ``inplace_backward`` the backward writes da into a's storage and db
+    into b's: a and b must not be used elsewhere after the backward (in an MLP
+    they are the gate/up projections' outputs, used only here)."""
+
+    @staticmethod
+    def forward(ctx, a, b, act: str = "silu", inplace_backward: bool = False):
+        y = _fwd(a, b, act=act)
+        ctx.save_for_backward(a, b)
+        ctx.act = act
+        ctx.inplace_backward = inplace_backward
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        a, b = ctx.saved_tensors
+        if dy.stride(-1) != 1:
+            dy = dy.contiguous()
+        da, db = _bwd(dy, a, b, act=ctx.act, inplace=ctx.inplace_backward)
+        return da, db, None, None
+
+
+class GLUConcatFunction(torch.autograd.Function):
+    """y = act(x[..., :I]) * x[..., I:] for one tensor holding [gate | up] per
+    row (the output of a fused gate/up projection); the gradient is dx = [da | db]."""
+
+    @staticmethod
+    def forward(ctx, x, act: str = "silu", inplace_backward: bool = False):
+        y = _fwd(x, layout="concat", act=act)
+        ctx.save_for_backward(x)
+        ctx.act = act
+        ctx.inplace_backward = inplace_backward
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        (x,) = ctx.saved_tensors
+        if dy.stride(-1) != 1:
+            dy = dy.contiguous()
+        dx = _bwd(dy, x, layout="concat", act=ctx.act, inplace=ctx.inplace_backward)
+        return dx, None, None
+
+
+def glu(a, b=None, act: str = "silu", inplace_backward: bool = False):
+    """Functional form: glu(a, b) for separate tensors, glu(x) for [gate | up]."""
+    _check_act(act)
+    if b is None:
+        return GLUConcatFunction.apply(a, act, inplace_backward)
+    return GLUFunction.apply(a, b, act, inplace_backward)
+
+
+class GLU(nn.Module):
+    """The gated activation as a module: forward(a, b) or forward(x) with x = [gate | up]."""
+
+    def __init__(self, act: str = "silu", inplace_backward: bool = False):
+        super().__init__()
+        self.act = _check_act(act)
+        self.inplace_backward = inplace_backward
+
+    def forward(self, a, b=None):
+        return glu(a, b, self.act, self.inplace_backward)
+
+    def extra_repr(self):
+        return f"act={self.act}, inplace_backward={self.inplace_backward}"
+
+
+class GatedMLP(nn.Module):
+    """down(act(x W_gate^T) * (x W_up^T)) with the projections as torch Linear
+    layers (no bias) and the gated activation from the library.  With
+    ``fused_gate_up`` the gate and up projections are one Linear of 2 * I
+    outputs whose result feeds the [gate | up] layout directly, so no split or
+    copy is needed between the projection and the activation."""
+
+    def __init__(self, hidden: int, intermediate: int, act: str = "silu", fused_gate_up: bool = True,
+                 device=None, dtype=None):
+        super().__init__()
+        kw = {"device": device, "dtype": dtype, "bias": False}
+        self.act = _check_act(act)
+        self.fused_gate_up = fused_gate_up
+        if fused_gate_up:
+            self.gate_up_proj = nn.Linear(hidden, 2 * intermediate, **kw)
+        else:
+            self.gate_proj = nn.Linear(hidden, intermediate, **kw)
+            self.up_proj = nn.Linear(hidden, intermediate, **kw)
+        self.down_proj = nn.Linear(intermediate, hidden, **kw)
+
+    def forward(self, x):
+        if self.fused_gate_up:
+            h = glu(self.gate_up_proj(x), act=self.act, inplace_backward=True)
+        else:
+            h = glu(self.gate_proj(x), self.up_proj(x), act=self.act, inplace_backward=True)
+        return self.down_proj(h)

@@ -1,0 +1,99 @@
+"""The autograd layer: GLUFunction / GLUConcatFunction gradients against the
+oracle (bit patterns under the 1-ulp bar), with and without the in-place
+backward, a torch fp64 autograd cross-check in f32, and the GatedMLP module
+against a plain PyTorch composition with the same weights."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import glu_activation_mlps_gb300 as glu
+from glu_activation_mlps_gb300 import autograd as ga
+import glu_synth
+from helpers import compare, to_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    glu.build()
+    glu.lib()
+    glu.glu_set_tuning(0, 0, 0, 0, 0)
+
+
+@pytest.mark.parametrize("inplace", [False, True])
+@pytest.mark.parametrize("act", ["silu", "gelu_erf", "gelu_tanh", "relu"])
+def test_split_function_gradients_match_oracle(orc, act, inplace):
+    dt, shape = "bf16", (3, 37, 1000)
+    rng = np.random.default_rng(31)
+    a = glu_synth.normal_bits(rng, shape, 2.0, dt)
+    b = glu_synth.normal_bits(rng, shape, 1.0, dt)
+    dy = glu_synth.normal_bits(rng, shape, 1.0, dt)
+    A = to_dev(a, dt).requires_grad_(True)
+    B = to_dev(b, dt).requires_grad_(True)
+    # a non-leaf copy so that the in-place backward may overwrite it
+    A2, B2 = A * 1, B * 1
+    y = ga.glu(A2, B2, act=act, inplace_backward=inplace)
+    compare(to_bits(y.detach(), dt), orc.fwd(act, dt, a, b), dt, what=f"{act} autograd y")
+    y.backward(to_dev(dy, dt))
+    da_o, db_o = orc.bwd(act, dt, dy, a, b)
+    compare(to_bits(A.grad, dt), da_o, dt, what=f"{act} autograd da")
+    compare(to_bits(B.grad, dt), db_o, dt, what=f"{act} autograd db")
+
+
+def test_concat_function_gradient_matches_oracle(orc):
+    dt, rows, cols = "bf16", 50, 1111
+    rng = np.random.default_rng(32)
+    x = glu_synth.normal_bits(rng, (rows, 2 * cols), 1.5, dt)
+    dy = glu_synth.normal_bits(rng, (rows, cols), 1.0, dt)
+    for inplace in (False, True):
+        X = to_dev(x, dt).requires_grad_(True)
+        y = ga.glu(X * 1, act="gelu_tanh", inplace_backward=inplace)
+        compare(to_bits(y.detach(), dt), orc.fwd_concat("gelu_tanh", dt, x, cols), dt, what="concat y")
+        y.backward(to_dev(dy, dt))
+        dx_o = orc.bwd_concat("gelu_tanh", dt, dy, x, cols)
+        compare(to_bits(X.grad, dt)[:, :cols], dx_o[:, :cols], dt, what="concat da")
+        compare(to_bits(X.grad, dt)[:, cols:], dx_o[:, cols:], dt, what="concat db")
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_erf", "gelu_tanh"])
+def test_f32_gradients_against_torch_fp64_autograd(act):
+    g = torch.Generator(device="cuda").manual_seed(3)
+    a = torch.randn(64, 513, device="cuda", generator=g) * 2
+    b = torch.randn(64, 513, device="cuda", generator=g)
+    dy = torch.randn(64, 513, device="cuda", generator=g)
+    A, B = a.clone().requires_grad_(True), b.clone().requires_grad_(True)
+    ga.glu(A, B, act=act).backward(dy)
+    fn = {"silu": F.silu, "gelu_erf": lambda t: F.gelu(t, approximate="none"),
+          "gelu_tanh": lambda t: F.gelu(t, approximate="tanh")}[act]
+    A64, B64 = a.double().requires_grad_(True), b.double().requires_grad_(True)
+    (fn(A64) * B64).backward(dy.double())
+    scale = (dy.double().abs() * (B64.detach().abs() + 1)).max()
+    assert (A.grad.double() - A64.grad).abs().max() / scale < 1e-5
+    assert (B.grad.double() - B64.grad).abs().max() / scale < 1e-5
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_gated_mlp_matches_plain_torch(fused):
+    torch.manual_seed(0)
+    hidden, inter = 256, 704
+    mlp = ga.GatedMLP(hidden, inter, act="silu", fused_gate_up=fused, device="cuda", dtype=torch.bfloat16)
+    x = torch.randn(8, 33, hidden, device="cuda", dtype=torch.bfloat16, requires_grad=True)
+    y = mlp(x)
+    # the same weights through plain PyTorch ops
+    if fused:
+        wg, wu = mlp.gate_up_proj.weight[:inter], mlp.gate_up_proj.weight[inter:]
+    else:
+        wg, wu = mlp.gate_proj.weight, mlp.up_proj.weight
+    xr = x.detach().clone().requires_grad_(True)
+    h = F.silu((xr @ wg.t()).float()) * (xr @ wu.t()).float()
+    yr = h.to(torch.bfloat16) @ mlp.down_proj.weight.t()
+    assert torch.allclose(y.float(), yr.float(), atol=2e-2, rtol=2e-2)
+    gy = torch.randn_like(y)
+    y.backward(gy)
+    yr.backward(gy)
+    assert torch.allclose(x.grad.float(), xr.grad.float(), atol=3e-2, rtol=3e-2)
+    assert mlp.down_proj.weight.grad is not None
