@@ -64,6 +64,8 @@ def lib():
             L.oracle_round_vec.argtypes = [ci, dp, dp, i64]
             L.oracle_encode_vec.argtypes = [ci, dp, vp, i64]
             L.oracle_decode_vec.argtypes = [ci, vp, dp, i64]
+            L.oracle_gemm_glu_at.argtypes = [ci, ci, vp, i64, vp, vp, i64, i64, vp, vp, i64, vp, dp, dp, dp, dp]
+            L.oracle_gemm_glu_at.restype = None
             L.oracle_sigmoid.argtypes = [ctypes.c_double]
             L.oracle_sigmoid.restype = ctypes.c_double
             for f in (L.oracle_fwd, L.oracle_bwd, L.oracle_bwd_da_scale, L.oracle_act_vec,
@@ -228,3 +230,31 @@ def bwd_threaded(act_name: str, dtype: str, dc, a, b, threads: int):
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(work, _row_blocks(v[1].shape[0], threads)))
     return da, db
+
+
+# ---- the gate/up projections with the activation applied ----------------------
+
+def gemm_glu_at(act_name: str, dtype: str, x, w_gate, w_up, ms, is_):
+    """y[m, i] = round(act(x[m] . w_gate[i]) * (x[m] . w_up[i])) at the listed
+    (m, i) pairs, with the exact (double) g and u and the sums of |products|.
+    x is M x K, the weights I x K (bit arrays, row-major, contiguous)."""
+    x, wg, wu = _bits(x, dtype), _bits(w_gate, dtype), _bits(w_up, dtype)
+    if wg.shape != wu.shape or x.shape[1] != wg.shape[1]:
+        raise ValueError("x is M x K and the weights I x K")
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    is_ = np.ascontiguousarray(is_, dtype=np.int64)
+    n = ms.size
+    y = np.empty(n, dtype=BITS_DTYPE[dtype])
+    g, u, sg, su = (np.empty(n) for _ in range(4))
+    lib().oracle_gemm_glu_at(ACTS[act_name], DTYPES[dtype], _ptr(x), x.shape[1], _ptr(wg), _ptr(wu),
+                             wg.shape[1], x.shape[1], _ptr(ms), _ptr(is_), n, _ptr(y), _ptr(g), _ptr(u),
+                             _ptr(sg), _ptr(su))
+    return y, g, u, sg, su
+
+
+def gemm_glu(act_name: str, dtype: str, x, w_gate, w_up):
+    """Every output: an M x I bit array (small problems only)."""
+    M, I = np.asarray(x).shape[0], np.asarray(w_gate).shape[0]
+    mm, ii = np.meshgrid(np.arange(M), np.arange(I), indexing="ij")
+    y, *_ = gemm_glu_at(act_name, dtype, x, w_gate, w_up, mm.ravel(), ii.ravel())
+    return y.reshape(M, I)

@@ -296,3 +296,49 @@ void oracle_decode_vec(int dtype, const void *bits, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_decode(load_bits(bits, i, dtype), dtype);
 }
+
+/* ------------------------------------------------------------------ */
+/* The gated MLP's first half with the activation applied to the projections
+ * ("Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel", Purpose: the MLP is
+ * down_proj(act(gate_proj(x)) * up_proj(x)); "Fused Kernels", section 4: the
+ * gate and up tiles computed as x @ gate^T and x @ up^T):
+ *   g[m,i] = sum_k x[m,k] * w_gate[i,k],   u[m,i] = sum_k x[m,k] * w_up[i,k]
+ *   y[m,i] = round(act(g[m,i]) * u[m,i])
+ * x is M x K, the weights are I x K (row i holds output feature i), all
+ * row-major with row strides in elements.  Sums in double, k in order. */
+static void gate_up_at(int dtype, const void *x, int64_t sx, const void *wg, const void *wu, int64_t sw,
+                       int64_t K, int64_t m, int64_t i, double *g, double *u, double *ag, double *au)
+{
+    double sg = 0.0, su = 0.0, tg = 0.0, tu = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double xv = oracle_decode(load_bits(x, m * sx + k, dtype), dtype);
+        double gv = xv * oracle_decode(load_bits(wg, i * sw + k, dtype), dtype);
+        double uv = xv * oracle_decode(load_bits(wu, i * sw + k, dtype), dtype);
+        sg += gv;
+        su += uv;
+        tg += fabs(gv);
+        tu += fabs(uv);
+    }
+    *g = sg;
+    *u = su;
+    *ag = tg;
+    *au = tu;
+}
+
+/* y for the listed (m, i) pairs (n of them), plus g, u and the sums of
+ * |products| (Sg, Su) that bound the error of any reordered summation.  Any
+ * of g, u, sg, su may be NULL. */
+void oracle_gemm_glu_at(int act, int dtype, const void *x, int64_t sx, const void *wg, const void *wu,
+                        int64_t sw, int64_t K, const int64_t *ms, const int64_t *is, int64_t n, void *y,
+                        double *g, double *u, double *sg, double *su)
+{
+    for (int64_t j = 0; j < n; ++j) {
+        double gv, uv, ag, au;
+        gate_up_at(dtype, x, sx, wg, wu, sw, K, ms[j], is[j], &gv, &uv, &ag, &au);
+        store_bits(y, j, dtype, oracle_encode(oracle_act(act, gv) * uv, dtype));
+        if (g) g[j] = gv;
+        if (u) u[j] = uv;
+        if (sg) sg[j] = ag;
+        if (su) su[j] = au;
+    }
+}

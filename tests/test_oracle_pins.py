@@ -384,3 +384,39 @@ def test_threaded_drivers_equal_serial(orc):
     g1 = orc.bwd("gelu_tanh", "bf16", d["dc"], d["a"], d["b"])
     g2 = orc.bwd_threaded("gelu_tanh", "bf16", d["dc"], d["a"], d["b"], threads=3)
     assert all(np.array_equal(p, q) for p, q in zip(g1, g2))
+
+
+# --------------------------------------------------------------------------- gate/up projections
+
+def test_gemm_glu_gate_and_up_match_numpy_matmul(orc):
+    """g and u are the projections x @ w^T: checked against numpy's float64
+    matmul, and y against the element-wise oracle applied to them."""
+    rng = np.random.default_rng(41)
+    M, K, I = 7, 96, 11
+    x = glu_synth.normal_bits(rng, (M, K), 1.0, "bf16")
+    wg = glu_synth.normal_bits(rng, (I, K), 0.1, "bf16")
+    wu = glu_synth.normal_bits(rng, (I, K), 0.1, "bf16")
+    xv, gv, uv = (orc.decode("bf16", t) for t in (x, wg, wu))
+    mm, ii = np.meshgrid(np.arange(M), np.arange(I), indexing="ij")
+    y, g, u, sg, su = orc.gemm_glu_at("silu", "bf16", x, wg, wu, mm.ravel(), ii.ravel())
+    assert np.allclose(g, (xv @ gv.T).ravel(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(u, (xv @ uv.T).ravel(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(sg, (np.abs(xv) @ np.abs(gv).T).ravel(), rtol=1e-13)
+    want = orc.round_to("bf16", orc.act("silu", g) * u)
+    assert np.array_equal(orc.decode("bf16", y), want)
+    # row i of the weights is output feature i: swapping the operands changes the result
+    y_sw, *_ = orc.gemm_glu_at("silu", "bf16", x, wu, wg, mm.ravel(), ii.ravel())
+    assert not np.array_equal(y, y_sw)
+
+
+def test_gemm_glu_exact_integer_case(orc):
+    """Small integers: every product and sum is exact, so g and u are known in
+    closed form (x = 1, weights = k-index pattern)."""
+    K = 8
+    x = orc.encode("bf16", np.ones((1, K)))
+    wg = orc.encode("bf16", np.arange(K, dtype=float)[None, :] - 3.0)       # sum = 28 - 24 = 4
+    wu = orc.encode("bf16", np.full((1, K), 0.5))                            # sum = 4
+    y, g, u, *_ = orc.gemm_glu_at("relu", "bf16", x, wg, wu, [0], [0])
+    assert g[0] == 4.0 and u[0] == 4.0 and orc.decode("bf16", y)[0] == 16.0
+    y2 = orc.gemm_glu("gelu_tanh", "bf16", x, wg, wu)
+    assert orc.decode("bf16", y2)[0, 0] == orc.round_to("bf16", orc.act("gelu_tanh", [4.0]) * 4.0)[0]
