@@ -31,7 +31,7 @@ STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STR
 EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_fwd_host_noalloc",
            "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
-           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts")
+           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_gemm_fwd")
 
 
 class GluError(RuntimeError):
@@ -105,6 +105,8 @@ def lib() -> ctypes.CDLL:
             L.glu_get_tuning.restype = ci
             L.glu_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
             L.glu_wait_timeouts.restype = ci
+            L.glu_gemm_fwd.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, i64, ci, ci, vp]
+            L.glu_gemm_fwd.restype = ci
             _lib = L
     return _lib
 
@@ -181,6 +183,10 @@ def glu_wait_timeouts(reset: bool = False) -> int:
     if st:
         raise GluError(st, "glu_wait_timeouts")
     return c.value
+
+
+def glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream) -> int:
+    return lib().glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream)
 
 
 def glu_get_tuning() -> dict:
@@ -303,6 +309,33 @@ def bwd(dc, a, b=None, *, da=None, db=None, act: str = "silu", layout: str = "sp
     if st:
         raise GluError(st, "glu_bwd")
     return da, db
+
+
+def gemm_fwd(x, w_gate, w_up, *, y=None, act: str = "silu", stream=None):
+    """y = act(x @ w_gate^T) * (x @ w_up^T) on the tensor cores, the activation
+    applied in the GEMM epilogue.  x is (..., K); the weights are (I, K) in the
+    nn.Linear layout and share one row stride; f16 or bf16."""
+    import torch
+    n_rows, x_stride = _rows(x, "x")
+    if w_gate.dim() != 2 or w_up.shape != w_gate.shape or w_gate.shape[1] != x.shape[-1]:
+        raise ValueError("w_gate and w_up must both be (I, K) with K = x.shape[-1]")
+    if w_gate.dtype != x.dtype or w_up.dtype != x.dtype:
+        raise ValueError("x and the weights must have one dtype")
+    _, wg_stride = _rows(w_gate, "w_gate")
+    _, wu_stride = _rows(w_up, "w_up")
+    if wg_stride != wu_stride:
+        raise ValueError("w_gate and w_up must have one row stride")
+    n_out, K = w_gate.shape
+    if y is None:
+        y = torch.empty((*x.shape[:-1], n_out), dtype=x.dtype, device=x.device)
+    if tuple(y.shape) != (*x.shape[:-1], n_out) or y.dtype != x.dtype:
+        raise ValueError("y has the wrong shape or dtype")
+    _, y_stride = _rows(y, "y")
+    st = glu_gemm_fwd(x.data_ptr(), x_stride, w_gate.data_ptr(), w_up.data_ptr(), wg_stride,
+                      y.data_ptr(), y_stride, n_rows, K, n_out, ACT[act], _dtype_code(x), _stream(stream))
+    if st:
+        raise GluError(st, "glu_gemm_fwd")
+    return y
 
 
 # ---- host tensors ---------------------------------------------------------------

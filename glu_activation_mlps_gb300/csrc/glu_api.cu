@@ -512,8 +512,12 @@ int glu_version(void) { return GLU_VERSION; }
 int glu_wait_timeouts(unsigned int *count, int reset)
 {
     if (!count) return GLU_ERR_NULL;
-    cudaError_t e = glu::bulk_timeouts(count, reset != 0);
-    return e == cudaSuccess ? GLU_OK : cuda_fail(e);
+    unsigned int bulk = 0, gemm = 0;
+    cudaError_t e = glu::bulk_timeouts(&bulk, reset != 0);
+    if (e == cudaSuccess) e = glu::gemm::timeouts(&gemm, reset != 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *count = bulk + gemm;
+    return GLU_OK;
 }
 
 int glu_last_launch(glu_launch_info_t *out)

@@ -82,6 +82,9 @@ BulkFn bulk_kernel(int dtype, int act, int dir, bool narrow);
 int bulk_smem_bytes(int dir, bool narrow);
 int bulk_threads(bool narrow);
 cudaError_t bulk_timeouts(unsigned int *count, bool reset);
+namespace gemm {
+cudaError_t timeouts(unsigned int *count, bool reset);   // glu_gemm.cu
+}
 
 // One validated call: what the planner needs.  Strides are in elements.
 struct Call {

@@ -119,3 +119,32 @@ def all_finite_16bit(dtype: str) -> np.ndarray:
     bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     exp_all_ones = (0x7C00 if dtype == "f16" else 0x7F80)
     return bits[(bits & exp_all_ones) != exp_all_ones]
+
+
+# ---------------------------------------------------------------------------
+# Gate/up projections with the activation in the epilogue.
+# ---------------------------------------------------------------------------
+
+GRID_EIGHTHS = np.array([-2.0, -1.0, 0.0, 1.0, 2.0], dtype=np.float32) / np.float32(8.0)
+
+
+def grid_bits(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
+    """Entries drawn uniformly from {-1/4, -1/8, 0, 1/8, 1/4}: every product is
+    a multiple of 2^-6 and every partial sum of up to 2^20 of them is exact in
+    fp32, whatever the order of the additions."""
+    idx = rng.integers(0, GRID_EIGHTHS.size, size=shape, dtype=np.int8)
+    return f32_to_bits(GRID_EIGHTHS[idx], dtype)
+
+
+def gemm_llama(seed: int = 7, M: int = 4096, K: int = 4096, I: int = 14336, dtype: str = "bf16",
+               exact: bool = False):
+    """Gate/up projections of one MLP: x (M, K) ~ N(0, 1), w_gate and w_up (I, K)
+    ~ N(0, 1/K) (the usual fan-in scale), in ``dtype``.  With ``exact`` every
+    operand is drawn from the grid of ``grid_bits`` instead."""
+    rng = np.random.default_rng([seed, M, K, I])
+    if exact:
+        return {"x": grid_bits(rng, (M, K), dtype), "w_gate": grid_bits(rng, (I, K), dtype),
+                "w_up": grid_bits(rng, (I, K), dtype), "dtype": dtype}
+    s = float(1.0 / np.sqrt(K))
+    return {"x": normal_bits(rng, (M, K), 1.0, dtype), "w_gate": normal_bits(rng, (I, K), s, dtype),
+            "w_up": normal_bits(rng, (I, K), s, dtype), "dtype": dtype}

@@ -39,7 +39,8 @@
  *     returns GLU_OK without launching (pointers may then be NULL).
  *   - Pointers and strides that are 32- or 16-byte aligned use 256- or 128-bit
  *     memory accesses; any other alignment is valid and uses element-wide
- *     accesses.  Alignment is never an error.
+ *     accesses.  Alignment is never an error, except for the operands that
+ *     glu_gemm_fwd reads through the tensor-memory accelerator.
  *   - Non-finite inputs are outside the numerical contract; they do not fault.
  */
 #ifndef GLU_H
@@ -278,12 +279,53 @@ typedef struct {
 int glu_set_tuning(const glu_tuning_t *t);   /* GLU_ERR_ENUM for unsupported values */
 int glu_get_tuning(glu_tuning_t *out);
 
-/* Kernels that wait on the bulk-copy engine bound every wait (about a second)
- * and count the waits that ran out on the current device instead of hanging.
+/* Kernels that wait on the bulk-copy engine or the tensor cores (the bulk-copy
+ * path and glu_gemm_fwd) bound every wait (about a second) and count the waits
+ * that ran out on the current device instead of hanging.
  * Copies that count into *count (synchronising with the device) and, if
  * `reset`, sets it back to 0.  A nonzero count means some outputs of those
  * launches were not written. */
 int glu_wait_timeouts(unsigned int *count, int reset);
+
+/*
+ * Gate and up projections with the gated activation applied in the GEMM
+ * epilogue, on the tensor cores:
+ *
+ *     y[m, i] = round(act(g[m, i]) * u[m, i]),
+ *     g[m, i] = sum_k x[m, k] * w_gate[i, k],   u[m, i] = sum_k x[m, k] * w_up[i, k].
+ *
+ * Sources: "Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel" (Purpose; "Versus
+ * epilogue fusion" under Performance requirements: the gate and up tiles stay
+ * on chip and only y reaches HBM) and "Fused Kernels" (section 4, "The fused
+ * MLP": gate and up tiles as x @ gate^T and x @ up^T, the activation applied
+ * to them in registers).  g and u are accumulated in fp32 (products of
+ * 16-bit values are exact in fp32; the order of the additions is the
+ * hardware's), then the activation runs in fp32 as in glu_fwd and the result
+ * is rounded to nearest-even once.
+ *
+ *   x, x_stride        M x K activations (row-major, element stride x_stride >= K).
+ *   w_gate, w_up       I x K weights, row i holding output feature i (the
+ *                      nn.Linear layout), both with row stride w_stride >= K.
+ *   y, y_stride        M x I output, y_stride >= I.  y must not overlap x or
+ *                      the weights (GLU_ERR_ALIAS).
+ *   act                any glu_act_t.
+ *   dtype              GLU_F16 or GLU_BF16 (the tensor cores take both operands
+ *                      in one 16-bit type); GLU_F32 returns GLU_ERR_ENUM.
+ *   stream             CUDA stream the kernel is enqueued on.
+ * The operands are read by the tensor-memory accelerator: x, w_gate and w_up
+ * must be 16-byte aligned and x_stride, w_stride multiples of 8 elements,
+ * else GLU_ERR_STRIDE (y has no alignment rule).  M, K, I < 2^31.  M == 0 or
+ * I == 0 returns GLU_OK without work; K == 0 sets y to 0 (act(0) * 0).
+ * All pointers are device pointers; the library keeps none after the call.
+ * A wait that runs out of its time budget (about a second) is counted for
+ * glu_wait_timeouts() and leaves that block's outputs unwritten.
+ * Returns GLU_OK or a negative glu_status_t.
+ */
+int glu_gemm_fwd(const void *x, int64_t x_stride,
+                 const void *w_gate, const void *w_up, int64_t w_stride,
+                 void *y, int64_t y_stride,
+                 int64_t M, int64_t K, int64_t I,
+                 glu_act_t act, glu_dtype_t dtype, glu_stream_t stream);
 
 #ifdef __cplusplus
 }

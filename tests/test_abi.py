@@ -229,3 +229,33 @@ def test_host_workspace_size_formula():
     assert ws(10, 1024, SPLIT, F16, 1) == 2 * 5 * 20480                       # dc, a, b | da, db
     assert ws(10, 1024, CONCAT, F16, 1) == 2 * (20480 + 40960 + 40960)        # dc, x | dx
     assert ws(0, 64, SPLIT, BF16, 0) == 0 and ws(4, 64, 9, BF16, 0) == 0
+
+
+# ---- glu_gemm_fwd -------------------------------------------------------------
+
+def gemm(x=BASE, sx=64, wg=BASE + (1 << 20), wu=BASE + (2 << 20), sw=64, y=BASE + (3 << 20), sy=96,
+         M=4, K=64, I=96, act=SILU, dtype=BF16):
+    return glu.glu_gemm_fwd(x, sx, wg, wu, sw, y, sy, M, K, I, act, dtype, None)
+
+
+def test_gemm_validation():
+    assert gemm(dtype=F32) == ENUM and gemm(dtype=3) == ENUM and gemm(act=4) == ENUM
+    assert gemm(M=-1) == SHAPE and gemm(K=-1) == SHAPE and gemm(I=1 << 31) == SHAPE
+    assert gemm(x=None, y=None, M=0) == OK and gemm(wg=None, I=0, y=None) == OK
+    assert gemm(x=None) == NULL and gemm(wu=None) == NULL and gemm(y=None) == NULL
+    assert gemm(sx=63) == STRIDE and gemm(sw=32) == STRIDE and gemm(sy=95) == STRIDE
+    # the tensor-memory accelerator's alignment rules: bases and row strides on 16 bytes
+    assert gemm(x=BASE + 2) == STRIDE and gemm(wg=BASE + (1 << 20) + 8) == STRIDE
+    assert gemm(sx=68) == STRIDE and gemm(sw=66) == STRIDE
+    # y over x, over either weight
+    assert gemm(y=BASE + 2) == ALIAS
+    assert gemm(y=BASE + (2 << 20) + 64 * 2 * 50) == ALIAS
+    assert gemm(y=BASE + (1 << 20) - 4) == ALIAS
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake addresses")
+def test_gemm_valid_call_reaches_the_cuda_runtime_without_a_gpu():
+    # y may be unaligned and strided; the inputs may overlap one another
+    assert gemm(y=BASE + (3 << 20) + 2, sy=101) == CUDA
+    assert gemm(wu=BASE + (1 << 20)) == CUDA
+    assert glu.glu_last_cuda_error()
