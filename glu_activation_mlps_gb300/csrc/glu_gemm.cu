@@ -8,20 +8,23 @@
 // and up tiles are still on chip, so they never reach HBM; "Fused Kernels",
 // section 4: gate and up tiles computed as x @ gate^T and x @ up^T.)
 //
-// One block computes a 128 x BN tile of y.  Warp 0 moves 64-wide K slices of x,
-// w_gate and w_up into a ring of shared-memory stages with the tensor-memory
-// accelerator (128-byte swizzle).  One thread of warp 1 issues tcgen05.mma
-// (kind::f16, M = 128, N = BN, K = 16) into two fp32 accumulators in tensor
-// memory, gate and up, and releases each stage with tcgen05.commit.  Warps 2-5
-// read both accumulators with tcgen05.ld (one row per thread), apply the same
-// fp32 activation as the streaming kernels, round once and store.  Blocks are
-// ordered in groups of eight row blocks so that weight tiles are reused from
-// L2 by the blocks running at the same time.
+// A persistent grid of one block per SM walks 128 x BN tiles of y.  Warp 0
+// moves 64-wide K slices of x, w_gate and w_up into a ring of shared-memory
+// stages with the tensor-memory accelerator (128-byte swizzle); the gate and
+// up slices sit back to back, so one tcgen05.mma of N = 2 BN (kind::f16,
+// M = 128, K = 16), issued by one thread of warp 1, accumulates both into one
+// fp32 [gate | up] block of tensor memory.  Tensor memory holds two such
+// blocks, so the MMAs of the next tile run while warps 2-5 read the finished
+// one with tcgen05.ld (one row per thread), apply the same fp32 activation as
+// the streaming kernels, round once and store.  Tiles are ordered in groups of
+// eight row blocks so that weight slices are reused from L2 by the blocks
+// running at the same time.
 //
 // Every wait is bounded by a clock budget (about a second); a wait that runs
-// out is counted in a device word (read by glu_wait_timeouts), stops the
-// block's producer and MMA issuer, waits (bounded) for the copies and MMAs it
-// already issued, frees its tensor memory and returns without storing.
+// out is counted in a device word (read by glu_wait_timeouts) and raises a
+// block-wide abort flag: every role leaves its loop, the producer and the MMA
+// issuer wait (bounded) for the copies and MMAs already issued, the block
+// frees its tensor memory and returns with the remaining tiles unwritten.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -40,18 +43,22 @@ constexpr int BM = 128;                  // rows of x per tile (tensor-memory la
 constexpr int BK = 64;                   // K per stage: 64 x 2 bytes = one 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kThreads = 192;            // warp 0 loads, warp 1 issues MMAs, warps 2-5 store
+constexpr int kEpiWarps = 4;
 constexpr long long kBudget = 2000000000LL;   // ~1 s at 2 GHz
 constexpr int kGroupM = 8;
 
 template <int BN>
 struct Shape {
     static constexpr int kTileA = BM * BK * 2;
-    static constexpr int kTileB = BN * BK * 2;
+    static constexpr int kTileB = BN * BK * 2;                    // one of gate, up
     static constexpr int kStageBytes = kTileA + 2 * kTileB;
-    static constexpr int kTmemCols = 2 * BN;                      // gate | up
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 16;
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    static constexpr int kAccCols = 2 * BN;                       // [gate | up] of one tile
+    static constexpr int kTmemCols = 2 * kAccCols;                // two tiles in flight
+    static constexpr int kBars = 2 * kStages + 2 + 2 + 1;         // full, empty, acc_full, acc_empty, done
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBars * 8 + 16;
+    static_assert(BN % 32 == 0 && BN >= 32 && 2 * BN <= 256, "one MMA covers N = 2 BN <= 256");
     static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
+    static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
 };
 
 struct Params {
@@ -152,6 +159,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "memory");
 }
 
+__device__ __forceinline__ void arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Tile t of the grouped order: eight row blocks side by side walk the column blocks.
+__device__ __forceinline__ void tile_origin(const Params &p, int t, int &m0, int &ib)
+{
+    const int per_group = kGroupM * p.i_blocks;
+    const int first_m = (t / per_group) * kGroupM;
+    const int gsize = min(p.m_blocks - first_m, kGroupM);
+    const int r = t % per_group;
+    m0 = (first_m + r % gsize) * BM;
+    ib = r / gsize;
+}
+
 template <class Act, class T, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     glu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
@@ -159,36 +182,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using S = Shape<BN>;
     using Cd = Codec<T>;
-    constexpr uint32_t kIdesc = idesc_f16(std::is_same<T, __nv_bfloat16>::value ? 1 : 0, BM, BN);
+    constexpr uint32_t kIdesc = idesc_f16(std::is_same<T, __nv_bfloat16>::value ? 1 : 0, BM, 2 * BN);
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = saddr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);     // 1024-byte aligned ring
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * S::kStageBytes);
     uint64_t *empty = full + kStages;
-    uint64_t *acc_full = empty + kStages;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(acc_full + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(acc_full + 1) + 1;
+    uint64_t *acc_full = empty + kStages;       // [2]: MMAs of a tile done
+    uint64_t *acc_empty = acc_full + 2;         // [2]: the epilogue has read a tile
+    uint64_t *done = acc_empty + 2;             // every MMA this block issued, done
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(done + 1) + 1;
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // grouped order: eight row blocks side by side walk the column blocks
-    const int pid = blockIdx.x;
-    const int per_group = kGroupM * p.i_blocks;
-    const int first_m = (pid / per_group) * kGroupM;
-    const int gsize = min(p.m_blocks - first_m, kGroupM);
-    const int mb = first_m + (pid % per_group) % gsize;
-    const int ib = (pid % per_group) / gsize;
-    const int m0 = mb * BM, i0 = ib * BN;
+    const int n_tiles = p.m_blocks * p.i_blocks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[s])) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&empty[s])) : "memory");
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(acc_full)) : "memory");
+        for (int b = 0; b < 2; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&acc_full[b])) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&acc_empty[b])), "r"(kEpiWarps)
+                         : "memory");
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(done)) : "memory");
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -208,79 +230,113 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued = 0;
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (*abort_flag) break;
-                const int s = kt % kStages;
-                if (kt >= kStages && !wait_parity(saddr(&empty[s]), uint32_t((kt / kStages - 1) & 1))) {
-                    atomicAdd(&g_gemm_timeouts, 1u);
-                    *abort_flag = 1;
-                    break;
+            // producer: stage s = it % kStages is reused for the (it / kStages)-th time
+            uint32_t it = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+                int m0, ib;
+                tile_origin(p, t, m0, ib);
+                const int i0 = ib * BN;
+                for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % kStages, use = it / kStages;
+                    if (*abort_flag) break;
+                    if (use > 0 && !wait_parity(saddr(&empty[s]), (use - 1) & 1)) {
+                        atomicAdd(&g_gemm_timeouts, 1u);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    unsigned char *st = smem + s * S::kStageBytes;
+                    const uint32_t bar = saddr(&full[s]);
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                                 "r"(uint32_t(S::kStageBytes))
+                                 : "memory");
+                    tma_load(saddr(st), &tm_x, kt * BK, m0, bar);
+                    tma_load(saddr(st + S::kTileA), &tm_wg, kt * BK, i0, bar);
+                    tma_load(saddr(st + S::kTileA + S::kTileB), &tm_wu, kt * BK, i0, bar);
                 }
-                unsigned char *st = smem + s * S::kStageBytes;
-                const uint32_t bar = saddr(&full[s]);
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                             "r"(uint32_t(S::kStageBytes))
-                             : "memory");
-                tma_load(saddr(st), &tm_x, kt * BK, m0, bar);
-                tma_load(saddr(st + S::kTileA), &tm_wg, kt * BK, i0, bar);
-                tma_load(saddr(st + S::kTileA + S::kTileB), &tm_wu, kt * BK, i0, bar);
-                issued = kt + 1;
             }
             // the block may only exit once every copy it issued has landed
-            const int first = issued > kStages ? issued - kStages : 0;
-            for (int kt = first; kt < issued; ++kt)
-                if (!wait_parity(saddr(&full[kt % kStages]), uint32_t((kt / kStages) & 1))) {
+            const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
+            for (uint32_t j = first; j < it; ++j)
+                if (!wait_parity(saddr(&full[j % kStages]), (j / kStages) & 1)) {
                     atomicAdd(&g_gemm_timeouts, 1u);
                     break;
                 }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            uint32_t it = 0;
+            int lt = 0;
+            for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
                 if (*abort_flag) break;
-                const int s = kt % kStages;
-                if (!wait_parity(saddr(&full[s]), uint32_t((kt / kStages) & 1))) {
+                const int ab = lt & 1, use_acc = lt >> 1;
+                if (use_acc > 0 && !wait_parity(saddr(&acc_empty[ab]), (use_acc - 1) & 1)) {
                     atomicAdd(&g_gemm_timeouts, 1u);
                     *abort_flag = 1;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = saddr(smem + s * S::kStageBytes);
-                const uint64_t da = desc_sw128(a0);
-                const uint64_t dg = desc_sw128(a0 + S::kTileA);
-                const uint64_t du = desc_sw128(a0 + S::kTileA + S::kTileB);
+                const uint32_t d = tmem + uint32_t(ab * S::kAccCols);
+                bool ok = true;
+                for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % kStages, use = it / kStages;
+                    if (!wait_parity(saddr(&full[s]), use & 1)) {
+                        atomicAdd(&g_gemm_timeouts, 1u);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a0 = saddr(smem + s * S::kStageBytes);
+                    const uint64_t da = desc_sw128(a0);
+                    const uint64_t db = desc_sw128(a0 + S::kTileA);    // gate rows, then up rows
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    // K advances by 16 elements = 32 bytes inside the swizzle row
-                    const uint64_t step = uint64_t(kk * 32 >> 4);
-                    const uint32_t acc = (kt | kk) != 0;
-                    mma(tmem, da + step, dg + step, kIdesc, acc);
-                    mma(tmem + BN, da + step, du + step, kIdesc, acc);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // K advances by 16 elements = 32 bytes inside the swizzle row
+                        const uint64_t step = uint64_t(kk * 32 >> 4);
+                        mma(d, da + step, db + step, kIdesc, (kt | kk) != 0);
+                    }
+                    mma_commit(saddr(&empty[s]));       // the stage is free once these MMAs finish
                 }
-                mma_commit(saddr(&empty[s]));       // the stage is free once these MMAs finish
+                if (!ok) break;
+                mma_commit(saddr(&acc_full[ab]));       // the tile's accumulator is complete
             }
-            mma_commit(saddr(acc_full));            // all MMAs issued so far, done
-            if (!wait_parity(saddr(acc_full), 0)) atomicAdd(&g_gemm_timeouts, 1u);
+            mma_commit(saddr(done));
+            if (!wait_parity(saddr(done), 0)) atomicAdd(&g_gemm_timeouts, 1u);
         }
     } else {
-        // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31
-        // tcgen05.ld is warp-collective: the whole warp takes one decision
-        const bool ok = __all_sync(0xFFFFFFFFu, wait_parity(saddr(acc_full), 0));
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (!ok) {
-            if (lane == 0) atomicAdd(&g_gemm_timeouts, 1u);
-        } else if (!*abort_flag) {
-            const int q = warp & 3;
-            const int row = q * 32 + lane;
-            const int m = m0 + row;
-            const uint32_t lane_base = uint32_t(q * 32) << 16;
+        // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31, one row per thread
+        const int q = warp & 3;
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        int lt = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
+            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+            const int ab = lt & 1, use_acc = lt >> 1;
+            // tcgen05.ld is warp-collective: the whole warp takes one decision
+            const bool ok = __all_sync(0xFFFFFFFFu, wait_parity(saddr(&acc_full[ab]), use_acc & 1));
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (!ok) {
+                if (lane == 0) {
+                    atomicAdd(&g_gemm_timeouts, 1u);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            int m0, ib;
+            tile_origin(p, t, m0, ib);
+            const int m = m0 + q * 32 + lane;
+            const int i0 = ib * BN;
+            const uint32_t acc = tmem + lane_base + uint32_t(ab * S::kAccCols);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t g[32], u[32];
-                tmem_ld32(tmem + lane_base + uint32_t(c0), g);
-                tmem_ld32(tmem + lane_base + uint32_t(BN + c0), u);
+                tmem_ld32(acc + uint32_t(c0), g);
+                tmem_ld32(acc + uint32_t(BN + c0), u);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (c0 + 32 == BN) {          // all of this tile read: hand the accumulator back
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) arrive(saddr(&acc_empty[ab]));
+                }
                 if (m >= p.M) continue;
                 uint32_t packed[32 / Cd::kPerWord];
 #pragma unroll
@@ -301,10 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         Access<16>::store(dst + 16 * v, w4);
                     }
                 } else {
-                    for (int j = 0; j < 32 && i + j < p.I; ++j) {
-                        const uint32_t w = packed[j / Cd::kPerWord];
-                        const float f = Cd::get(w, j % Cd::kPerWord);
-                        Cd::store1(dst + j * int64_t(sizeof(T)), f);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (i + j < p.I)
+                            Cd::store1(dst + j * int64_t(sizeof(T)), Cd::get(packed[j / Cd::kPerWord], j % Cd::kPerWord));
                     }
                 }
             }
@@ -459,8 +515,13 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     p.m_blocks = int((M + BM - 1) / BM);
     p.i_blocks = int((I + bn - 1) / bn);
     p.vec_store = (uintptr_t(y) % 16 == 0) && ((y_stride * E) % 16 == 0);
-    const int64_t blocks = int64_t(p.m_blocks) * p.i_blocks;
-    if (blocks > INT32_MAX) return GLU_ERR_SHAPE;
+    const int64_t tiles = int64_t(p.m_blocks) * p.i_blocks;
+    if (tiles > INT32_MAX) return GLU_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
+    const int64_t blocks = tiles < sms ? tiles : sms;     // persistent: one block per SM
 
     void *args[] = {&tx, &tg, &tu, &p};
     cudaLaunchConfig_t cfg{};
@@ -473,7 +534,7 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         cfg.attrs = nullptr;
