@@ -8,23 +8,32 @@
 // and up tiles are still on chip, so they never reach HBM; "Fused Kernels",
 // section 4: gate and up tiles computed as x @ gate^T and x @ up^T.)
 //
-// A persistent grid of one block per SM walks 128 x BN tiles of y.  Warp 0
-// moves 64-wide K slices of x, w_gate and w_up into a ring of shared-memory
-// stages with the tensor-memory accelerator (128-byte swizzle); the gate and
-// up slices sit back to back, so one tcgen05.mma of N = 2 BN (kind::f16,
-// M = 128, K = 16), issued by one thread of warp 1, accumulates both into one
-// fp32 [gate | up] block of tensor memory.  Tensor memory holds two such
-// blocks, so the MMAs of the next tile run while warps 2-5 read the finished
-// one with tcgen05.ld (one row per thread), apply the same fp32 activation as
-// the streaming kernels, round once and store.  Tiles are ordered in groups of
-// eight row blocks so that weight slices are reused from L2 by the blocks
-// running at the same time.
+// A persistent grid walks tiles of y, BN columns wide.  Each block has three
+// roles.  Warp 0 moves 64-wide K slices into a ring of shared-memory stages
+// with the tensor-memory accelerator (128-byte swizzle).  One thread of warp 1
+// issues tcgen05.mma (kind::f16, K = 16) into an fp32 [gate | up] accumulator
+// of 2 BN tensor-memory columns per row; tensor memory holds two of them, so
+// the MMAs of the next tile run while warps 2-5 read the finished one with
+// tcgen05.ld (one row per thread), apply the same fp32 activation as the
+// streaming kernels, round once and store.
+//
+// Two shapes:
+//   * one block per tile of 128 rows: the stage holds the x slice and the gate
+//     and up slices back to back, and one MMA of N = 2 BN covers both;
+//   * a cluster of two blocks per tile of 256 rows (cta_group::2): each block
+//     loads its own 128 rows of x, block 0 the gate slice and block 1 the up
+//     slice, and block 0 issues MMAs of M = 256, N = 2 BN that read the x rows
+//     of both blocks and the gate and up halves of N from one block each; each
+//     block's tensor memory receives [gate | up] for its own rows.  Every weight
+//     byte crosses L2 -> shared memory once per 256 rows instead of once per 128.
+// Tiles are ordered in groups of row blocks that share the weight slices in
+// flight, so the weights stream from HBM about once.
 //
 // Every wait is bounded by a clock budget (about a second); a wait that runs
-// out is counted in a device word (read by glu_wait_timeouts) and raises a
-// block-wide abort flag: every role leaves its loop, the producer and the MMA
-// issuer wait (bounded) for the copies and MMAs already issued, the block
-// frees its tensor memory and returns with the remaining tiles unwritten.
+// out is counted in a device word (read by glu_wait_timeouts) and raises the
+// abort flag of the block (and of its partner): every role leaves its loop, the
+// copies and MMAs already issued are waited for (bounded), tensor memory is
+// freed and the block returns with the remaining tiles unwritten.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,26 +48,30 @@
 namespace glu {
 namespace gemm {
 
-constexpr int BM = 128;                  // rows of x per tile (tensor-memory lanes)
+constexpr int BM = 128;                  // rows of x per block (tensor-memory lanes)
 constexpr int BK = 64;                   // K per stage: 64 x 2 bytes = one 128-byte swizzle row
-constexpr int kStages = 4;
 constexpr int kThreads = 192;            // warp 0 loads, warp 1 issues MMAs, warps 2-5 store
 constexpr int kEpiWarps = 4;
+constexpr int kRingBytes = 192 * 1024;   // shared memory given to the stage ring
 constexpr long long kBudget = 2000000000LL;   // ~1 s at 2 GHz
-constexpr int kGroupM = 8;
 
-template <int BN>
+template <int BN, int CTAS>
 struct Shape {
     static constexpr int kTileA = BM * BK * 2;
-    static constexpr int kTileB = BN * BK * 2;                    // one of gate, up
-    static constexpr int kStageBytes = kTileA + 2 * kTileB;
-    static constexpr int kAccCols = 2 * BN;                       // [gate | up] of one tile
-    static constexpr int kTmemCols = 2 * kAccCols;                // two tiles in flight
-    static constexpr int kBars = 2 * kStages + 2 + 2 + 1;         // full, empty, acc_full, acc_empty, done
+    static constexpr int kTileB = BN * BK * 2;                        // one of gate, up
+    static constexpr int kStageBytes = kTileA + (CTAS == 1 ? 2 : 1) * kTileB;
+    static constexpr int kStages = kRingBytes / kStageBytes > 8 ? 8 : kRingBytes / kStageBytes;
+    static constexpr int kMmaM = BM * CTAS;
+    static constexpr int kMmaN = 2 * BN;
+    static constexpr int kAccCols = 2 * BN;                           // [gate | up] of one tile
+    static constexpr int kTmemCols = 2 * kAccCols;                    // two tiles in flight
+    static constexpr int kBars = 2 * kStages + 2 + 2 + 1;             // full, empty, acc_full, acc_empty, done
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBars * 8 + 16;
-    static_assert(BN % 32 == 0 && BN >= 32 && 2 * BN <= 256, "one MMA covers N = 2 BN <= 256");
-    static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
+    static_assert(CTAS == 1 || CTAS == 2, "one block or a pair");
+    static_assert(BN % 32 == 0 && BN >= 32 && kMmaN <= 256, "one MMA covers N = 2 BN <= 256");
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "a power-of-two column count");
     static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 };
 
 struct Params {
@@ -66,7 +79,8 @@ struct Params {
     int64_t y_stride;       // bytes
     int M, I, K;
     int k_tiles;
-    int m_blocks, i_blocks;
+    int m_blocks, i_blocks; // row blocks of 128 * CTAS rows, column blocks of BN
+    int group_m;            // row blocks per group of the tile order
     int vec_store;          // y rows and base 16-byte aligned
 };
 
@@ -94,6 +108,41 @@ __device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity)
     }
 }
 
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared::cluster address of the same shared variable in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void arrive_local(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void arrive_expect_tx_local(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major tile stored as 128-byte rows
 // with the 128-byte swizzle: start address, leading byte offset (unused for
 // swizzled K-major tiles, encoded 1), stride byte offset 1024 (eight rows form
@@ -118,29 +167,81 @@ __host__ __device__ constexpr uint32_t idesc_f16(int ab_format, int M, int N)
            (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// 2-D tiled copy into this block's shared memory; the barrier may belong to
+// the partner block when CTAS == 2.
+template <int CTAS>
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
 {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
+    if constexpr (CTAS == 1)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+            "[%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+            "{%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+            : "memory");
 }
 
+template <int CTAS>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+    if constexpr (CTAS == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc)
+            : "memory");
 }
 
+// Arrive on `bar` (same offset in every block of the pair) once all MMAs this
+// thread issued so far are done.
+template <int CTAS>
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    if constexpr (CTAS == 1)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                bar),
+            "h"(uint16_t(3))
+            : "memory");
+}
+
+template <int CTAS>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols)
+{
+    if constexpr (CTAS == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+}
+
+template <int CTAS>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols)
+{
+    if constexpr (CTAS == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
 }
 
 // 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
@@ -159,55 +260,64 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "memory");
 }
 
-__device__ __forceinline__ void arrive(uint32_t bar)
+// Tile t of the grouped order: group_m row blocks side by side walk the column blocks.
+__device__ __forceinline__ void tile_origin(const Params &p, int t, int &mb, int &ib)
 {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Tile t of the grouped order: eight row blocks side by side walk the column blocks.
-__device__ __forceinline__ void tile_origin(const Params &p, int t, int &m0, int &ib)
-{
-    const int per_group = kGroupM * p.i_blocks;
-    const int first_m = (t / per_group) * kGroupM;
-    const int gsize = min(p.m_blocks - first_m, kGroupM);
+    const int per_group = p.group_m * p.i_blocks;
+    const int first_m = (t / per_group) * p.group_m;
+    const int gsize = min(p.m_blocks - first_m, p.group_m);
     const int r = t % per_group;
-    m0 = (first_m + r % gsize) * BM;
+    mb = first_m + r % gsize;
     ib = r / gsize;
 }
 
-template <class Act, class T, int BN>
+template <class Act, class T, int BN, int CTAS>
 __global__ void __launch_bounds__(kThreads, 1)
     glu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
                     const __grid_constant__ CUtensorMap tm_wu, const Params p)
 {
-    using S = Shape<BN>;
+    using S = Shape<BN, CTAS>;
     using Cd = Codec<T>;
-    constexpr uint32_t kIdesc = idesc_f16(std::is_same<T, __nv_bfloat16>::value ? 1 : 0, BM, 2 * BN);
+    constexpr int ST = S::kStages;
+    constexpr uint32_t kIdesc = idesc_f16(std::is_same<T, __nv_bfloat16>::value ? 1 : 0, S::kMmaM, S::kMmaN);
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = saddr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);     // 1024-byte aligned ring
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * S::kStageBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *acc_full = empty + kStages;       // [2]: MMAs of a tile done
-    uint64_t *acc_empty = acc_full + 2;         // [2]: the epilogue has read a tile
-    uint64_t *done = acc_empty + 2;             // every MMA this block issued, done
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ST * S::kStageBytes);
+    uint64_t *empty = full + ST;
+    uint64_t *acc_full = empty + ST;            // [2]: MMAs of a tile done
+    uint64_t *acc_empty = acc_full + 2;         // [2]: the epilogue (of both blocks) has read a tile
+    uint64_t *done = acc_empty + 2;             // every MMA issued for this block, done
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(done + 1) + 1;
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = CTAS == 1 ? 0u : cluster_rank();
+    const int cluster = blockIdx.x / CTAS, n_clusters = gridDim.x / CTAS;
     const int n_tiles = p.m_blocks * p.i_blocks;
 
+    // a timed-out wait stops this block and its partner
+    auto raise_abort = [&]() {
+        atomicAdd(&g_gemm_timeouts, 1u);
+        *abort_flag = 1;
+        if constexpr (CTAS == 2) {
+            const uint32_t peer = mapa(saddr(const_cast<int *>(abort_flag)), rank ^ 1u);
+            asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1) : "memory");
+        }
+    };
+
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < ST; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[s])) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&empty[s])) : "memory");
         }
         for (int b = 0; b < 2; ++b) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&acc_full[b])) : "memory");
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&acc_empty[b])), "r"(kEpiWarps)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&acc_empty[b])),
+                         "r"(kEpiWarps * CTAS)
                          : "memory");
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(done)) : "memory");
@@ -215,92 +325,104 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         saddr(const_cast<uint32_t *>(tmem_slot))),
-                     "r"(S::kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc<CTAS>(saddr(const_cast<uint32_t *>(tmem_slot)), S::kTmemCols);
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    if constexpr (CTAS == 2)
+        cluster_sync();         // the partner's barriers are initialised before any copy signals them
+    else
+        __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         if (lane == 0) {
-            // producer: stage s = it % kStages is reused for the (it / kStages)-th time
+            // producer: stage s = it % ST is filled for the (it / ST)-th time
             uint32_t it = 0;
-            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                int m0, ib;
-                tile_origin(p, t, m0, ib);
-                const int i0 = ib * BN;
+            for (int t = cluster; t < n_tiles && !*abort_flag; t += n_clusters) {
+                int mb, ib;
+                tile_origin(p, t, mb, ib);
+                const int m0 = mb * S::kMmaM + int(rank) * BM, i0 = ib * BN;
                 for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-                    const uint32_t s = it % kStages, use = it / kStages;
+                    const uint32_t s = it % ST, use = it / ST;
                     if (*abort_flag) break;
                     if (use > 0 && !wait_parity(saddr(&empty[s]), (use - 1) & 1)) {
-                        atomicAdd(&g_gemm_timeouts, 1u);
-                        *abort_flag = 1;
+                        raise_abort();
                         break;
                     }
-                    unsigned char *st = smem + s * S::kStageBytes;
-                    const uint32_t bar = saddr(&full[s]);
-                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                                 "r"(uint32_t(S::kStageBytes))
-                                 : "memory");
-                    tma_load(saddr(st), &tm_x, kt * BK, m0, bar);
-                    tma_load(saddr(st + S::kTileA), &tm_wg, kt * BK, i0, bar);
-                    tma_load(saddr(st + S::kTileA + S::kTileB), &tm_wu, kt * BK, i0, bar);
+                    const uint32_t st = saddr(smem + s * S::kStageBytes);
+                    if constexpr (CTAS == 1) {
+                        const uint32_t bar = saddr(&full[s]);
+                        arrive_expect_tx_local(bar, uint32_t(S::kStageBytes));
+                        tma_load<1>(st, &tm_x, kt * BK, m0, bar);
+                        tma_load<1>(st + S::kTileA, &tm_wg, kt * BK, i0, bar);
+                        tma_load<1>(st + S::kTileA + S::kTileB, &tm_wu, kt * BK, i0, bar);
+                    } else {
+                        // both blocks' copies count on block 0's barrier, which
+                        // alone arrives, expecting the bytes of the pair (block
+                        // 1's copies may land first: the phase cannot complete
+                        // before that arrival)
+                        uint32_t bar = saddr(&full[s]);
+                        if (rank == 0)
+                            arrive_expect_tx_local(bar, uint32_t(2 * S::kStageBytes));
+                        else
+                            bar = mapa(bar, 0);
+                        tma_load<2>(st, &tm_x, kt * BK, m0, bar);
+                        tma_load<2>(st + S::kTileA, rank == 0 ? &tm_wg : &tm_wu, kt * BK, i0, bar);
+                    }
                 }
             }
-            // the block may only exit once every copy it issued has landed
-            const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
-            for (uint32_t j = first; j < it; ++j)
-                if (!wait_parity(saddr(&full[j % kStages]), (j / kStages) & 1)) {
-                    atomicAdd(&g_gemm_timeouts, 1u);
-                    break;
-                }
+            // block 0 holds the barriers of every copy of the pair: wait for the
+            // last ones to land before the block may exit
+            if (rank == 0) {
+                const uint32_t first = it > uint32_t(ST) ? it - ST : 0;
+                for (uint32_t j = first; j < it; ++j)
+                    if (!wait_parity(saddr(&full[j % ST]), (j / ST) & 1)) {
+                        atomicAdd(&g_gemm_timeouts, 1u);
+                        break;
+                    }
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t it = 0;
-            int lt = 0;
-            for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
-                if (*abort_flag) break;
-                const int ab = lt & 1, use_acc = lt >> 1;
-                if (use_acc > 0 && !wait_parity(saddr(&acc_empty[ab]), (use_acc - 1) & 1)) {
-                    atomicAdd(&g_gemm_timeouts, 1u);
-                    *abort_flag = 1;
-                    break;
-                }
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t d = tmem + uint32_t(ab * S::kAccCols);
-                bool ok = true;
-                for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-                    const uint32_t s = it % kStages, use = it / kStages;
-                    if (!wait_parity(saddr(&full[s]), use & 1)) {
-                        atomicAdd(&g_gemm_timeouts, 1u);
-                        *abort_flag = 1;
-                        ok = false;
+            if (rank == 0) {
+                uint32_t it = 0;
+                int lt = 0;
+                for (int t = cluster; t < n_tiles; t += n_clusters, ++lt) {
+                    if (*abort_flag) break;
+                    const int ab = lt & 1, use_acc = lt >> 1;
+                    if (use_acc > 0 && !wait_parity(saddr(&acc_empty[ab]), (use_acc - 1) & 1)) {
+                        raise_abort();
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t a0 = saddr(smem + s * S::kStageBytes);
-                    const uint64_t da = desc_sw128(a0);
-                    const uint64_t db = desc_sw128(a0 + S::kTileA);    // gate rows, then up rows
+                    const uint32_t d = tmem + uint32_t(ab * S::kAccCols);
+                    bool ok = true;
+                    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+                        const uint32_t s = it % ST, use = it / ST;
+                        if (!wait_parity(saddr(&full[s]), use & 1)) {
+                            raise_abort();
+                            ok = false;
+                            break;
+                        }
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        const uint32_t a0 = saddr(smem + s * S::kStageBytes);
+                        const uint64_t da = desc_sw128(a0);
+                        const uint64_t db = desc_sw128(a0 + S::kTileA);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // K advances by 16 elements = 32 bytes inside the swizzle row
-                        const uint64_t step = uint64_t(kk * 32 >> 4);
-                        mma(d, da + step, db + step, kIdesc, (kt | kk) != 0);
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            // K advances by 16 elements = 32 bytes inside the swizzle row
+                            const uint64_t step = uint64_t(kk * 32 >> 4);
+                            mma<CTAS>(d, da + step, db + step, kIdesc, (kt | kk) != 0);
+                        }
+                        mma_commit<CTAS>(saddr(&empty[s]));     // the stage is free once these MMAs finish
                     }
-                    mma_commit(saddr(&empty[s]));       // the stage is free once these MMAs finish
+                    if (!ok) break;
+                    mma_commit<CTAS>(saddr(&acc_full[ab]));     // the tile's accumulator is complete
                 }
-                if (!ok) break;
-                mma_commit(saddr(&acc_full[ab]));       // the tile's accumulator is complete
+                mma_commit<CTAS>(saddr(done));
             }
-            mma_commit(saddr(done));
+            // no MMA may still read this block's shared memory or write its tensor memory
             if (!wait_parity(saddr(done), 0)) atomicAdd(&g_gemm_timeouts, 1u);
         }
     } else {
@@ -308,22 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
         int lt = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
+        for (int t = cluster; t < n_tiles; t += n_clusters, ++lt) {
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             const int ab = lt & 1, use_acc = lt >> 1;
             // tcgen05.ld is warp-collective: the whole warp takes one decision
             const bool ok = __all_sync(0xFFFFFFFFu, wait_parity(saddr(&acc_full[ab]), use_acc & 1));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (!ok) {
-                if (lane == 0) {
-                    atomicAdd(&g_gemm_timeouts, 1u);
-                    *abort_flag = 1;
-                }
+                if (lane == 0) raise_abort();
                 break;
             }
-            int m0, ib;
-            tile_origin(p, t, m0, ib);
-            const int m = m0 + q * 32 + lane;
+            int mb, ib;
+            tile_origin(p, t, mb, ib);
+            const int m = mb * S::kMmaM + int(rank) * BM + q * 32 + lane;
             const int i0 = ib * BN;
             const uint32_t acc = tmem + lane_base + uint32_t(ab * S::kAccCols);
 #pragma unroll 1
@@ -335,7 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (c0 + 32 == BN) {          // all of this tile read: hand the accumulator back
                     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                     __syncwarp();
-                    if (lane == 0) arrive(saddr(&acc_empty[ab]));
+                    if (lane == 0) {
+                        if constexpr (CTAS == 1)
+                            arrive_local(saddr(&acc_empty[ab]));
+                        else
+                            arrive_cluster(mapa(saddr(&acc_empty[ab]), 0));
+                    }
                 }
                 if (m >= p.M) continue;
                 uint32_t packed[32 / Cd::kPerWord];
@@ -360,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         if (i + j < p.I)
-                            Cd::store1(dst + j * int64_t(sizeof(T)), Cd::get(packed[j / Cd::kPerWord], j % Cd::kPerWord));
+                            Cd::store1(dst + j * int64_t(sizeof(T)),
+                                       Cd::get(packed[j / Cd::kPerWord], j % Cd::kPerWord));
                     }
                 }
             }
@@ -368,12 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    if constexpr (CTAS == 2)
+        cluster_sync();         // neither block leaves while the other may still signal its barriers
+    else
+        __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 1) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::kTmemCols)
-                     : "memory");
+        tmem_dealloc<CTAS>(tmem, S::kTmemCols);
     }
 }
 
@@ -427,17 +554,40 @@ bool make_map(CUtensorMap *m, bool bf16, const void *base, int64_t rows, int64_t
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
-template <class T, int BN>
-KernelFn pick(int act)
+template <class T, int BN, int CTAS>
+KernelFn pick_act(int act)
 {
     switch (act) {
-    case 0: return glu_gemm_kernel<Silu, T, BN>;
-    case 1: return glu_gemm_kernel<GeluErf, T, BN>;
-    case 2: return glu_gemm_kernel<GeluTanh, T, BN>;
-    case 3: return glu_gemm_kernel<Relu, T, BN>;
+    case 0: return glu_gemm_kernel<Silu, T, BN, CTAS>;
+    case 1: return glu_gemm_kernel<GeluErf, T, BN, CTAS>;
+    case 2: return glu_gemm_kernel<GeluTanh, T, BN, CTAS>;
+    case 3: return glu_gemm_kernel<Relu, T, BN, CTAS>;
     default: return nullptr;
     }
 }
+
+struct Variant {
+    KernelFn fn;
+    int smem;
+};
+
+template <int BN, int CTAS>
+Variant variant(bool bf16, int act)
+{
+    return {bf16 ? pick_act<__nv_bfloat16, BN, CTAS>(act) : pick_act<__half, BN, CTAS>(act),
+            Shape<BN, CTAS>::kSmemBytes};
+}
+
+Variant pick(bool bf16, int act, int bn, int ctas)
+{
+    if (bn == 64) return ctas == 1 ? variant<64, 1>(bf16, act) : variant<64, 2>(bf16, act);
+    return ctas == 1 ? variant<128, 1>(bf16, act) : variant<128, 2>(bf16, act);
+}
+
+// Per kernel variant and device: the shared-memory opt-in done, and how many
+// blocks (one shape) or pairs (the other) fit on the GPU at once.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_slots[kMaxDevices][2][4][2][2];
 
 bool overlap(uintptr_t a0, uint64_t alen, uintptr_t b0, uint64_t blen)
 {
@@ -466,7 +616,10 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     using namespace glu::gemm;
     if (act < GLU_ACT_SILU || act > GLU_ACT_RELU || (dtype != GLU_F16 && dtype != GLU_BF16)) return GLU_ERR_ENUM;
     if (M < 0 || K < 0 || I < 0 || M > INT32_MAX || K > INT32_MAX || I > INT32_MAX) return GLU_ERR_SHAPE;
-    if (M == 0 || I == 0) return GLU_OK;
+    if (M == 0 || I == 0) {
+        glu::record_launch(glu_launch_info_t{});
+        return GLU_OK;
+    }
     if (!y || (K > 0 && (!x || !w_gate || !w_up))) return GLU_ERR_NULL;
     const int E = 2;
     if (y_stride < I || (K > 0 && (x_stride < K || w_stride < K))) return GLU_ERR_STRIDE;
@@ -474,7 +627,9 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     const uint64_t ylen = (uint64_t(M - 1) * uint64_t(y_stride) + uint64_t(I)) * E;
     if (K == 0) {   // empty sums: y = act(0) * 0 = 0
         cudaError_t e = cudaMemset2DAsync(y, size_t(y_stride) * E, 0, size_t(I) * E, size_t(M), s);
-        return e == cudaSuccess ? GLU_OK : glu::cuda_fail(e);
+        if (e != cudaSuccess) return glu::cuda_fail(e);
+        glu::record_launch(glu_launch_info_t{});
+        return GLU_OK;
     }
     // the tensor-memory accelerator needs 16-byte aligned bases and row strides
     if (uintptr_t(x) % 16 || uintptr_t(w_gate) % 16 || uintptr_t(w_up) % 16 || (x_stride * E) % 16 ||
@@ -488,16 +643,46 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
 
     const bool bf16 = dtype == GLU_BF16;
     const int bn = I <= 64 ? 64 : 128;
-    KernelFn fn = bn == 64 ? (bf16 ? pick<__nv_bfloat16, 64>(act) : pick<__half, 64>(act))
-                           : (bf16 ? pick<__nv_bfloat16, 128>(act) : pick<__half, 128>(act));
-    const int smem = bn == 64 ? Shape<64>::kSmemBytes : Shape<128>::kSmemBytes;
-    static std::atomic<int> smem_set[2][4][2];
-    std::atomic<int> &flag = smem_set[bf16][act][bn == 128];
-    if (!flag.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int ctas = M > BM ? 2 : 1;          // a pair of blocks per 256 rows once there are two row blocks
+    const Variant v = pick(bf16, act, bn, ctas);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
+
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(ctas);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(v.smem);
+    cfg.stream = s;
+
+    std::atomic<int> &slots = g_slots[dev % kMaxDevices][bf16][act][bn == 128][ctas == 2];
+    int n_slots = slots.load(std::memory_order_acquire);
+    if (n_slots == 0) {
+        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(v.fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 v.smem);
         if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
-        flag.store(1, std::memory_order_release);
+        n_slots = sms;
+        if (ctas == 2) {
+            cudaLaunchConfig_t q = cfg;
+            q.gridDim = dim3(unsigned(sms - sms % 2));
+            q.attrs = &attr[1];
+            q.numAttrs = 1;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(v.fn), &q);
+            if (e != cudaSuccess || clusters <= 0) {
+                (void)cudaGetLastError();
+                clusters = sms / 2;
+            }
+            n_slots = clusters;
+        }
+        slots.store(n_slots, std::memory_order_release);
     }
 
     CUtensorMap tx, tg, tu;
@@ -512,35 +697,40 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     p.I = int(I);
     p.K = int(K);
     p.k_tiles = int((K + BK - 1) / BK);
-    p.m_blocks = int((M + BM - 1) / BM);
+    const int64_t rows_per_block = int64_t(BM) * ctas;
+    p.m_blocks = int((M + rows_per_block - 1) / rows_per_block);
     p.i_blocks = int((I + bn - 1) / bn);
+    // row blocks per group: their x rows (about 48 MiB at most) stay in L2
+    // while the weight slices stream past them once
+    const int64_t block_bytes = rows_per_block * K * E;
+    int64_t group = (int64_t(48) << 20) / block_bytes;
+    group = group < 1 ? 1 : (group > p.m_blocks ? p.m_blocks : group);
+    p.group_m = int(group);
     p.vec_store = (uintptr_t(y) % 16 == 0) && ((y_stride * E) % 16 == 0);
     const int64_t tiles = int64_t(p.m_blocks) * p.i_blocks;
-    if (tiles > INT32_MAX) return GLU_ERR_SHAPE;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
-    const int64_t blocks = tiles < sms ? tiles : sms;     // persistent: one block per SM
+    if (tiles * ctas > INT32_MAX) return GLU_ERR_SHAPE;
+    const int64_t clusters = tiles < n_slots ? tiles : n_slots;     // persistent
 
     void *args[] = {&tx, &tg, &tu, &p};
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(blocks));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = size_t(smem);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(unsigned(clusters * ctas));
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
-    if (e != cudaSuccess) {
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(v.fn), args);
+    if (e != cudaSuccess) {     // retry without the dependent-launch attribute
         (void)cudaGetLastError();
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
-        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+        cfg.attrs = &attr[1];
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(v.fn), args);
     }
     if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
+    glu_launch_info_t info{};
+    info.launched = 1;
+    info.vec_bytes = p.vec_store ? 16 : E;
+    info.unroll = ctas;
+    info.threads = kThreads;
+    info.grid = int32_t(clusters * ctas);
+    info.path = 3;
+    info.vector_units = tiles;
+    glu::record_launch(info);
     return GLU_OK;
 }

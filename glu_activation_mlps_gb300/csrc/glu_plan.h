@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "glu.h"
+
 namespace glu {
 
 // One call's work, in bytes and access units.  A "unit" is one full-width
@@ -85,6 +87,7 @@ cudaError_t bulk_timeouts(unsigned int *count, bool reset);
 namespace gemm {
 cudaError_t timeouts(unsigned int *count, bool reset);   // glu_gemm.cu
 }
+void record_launch(const glu_launch_info_t &info);       // this thread's glu_last_launch
 
 // One validated call: what the planner needs.  Strides are in elements.
 struct Call {

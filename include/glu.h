@@ -233,8 +233,12 @@ const char *glu_last_cuda_error(void);
 /* GLU_VERSION of the loaded library. */
 int glu_version(void);
 
-/* What this thread's most recent successful glu_fwd / glu_bwd enqueued.
- * `launched` is 0 when the call was a no-op (an empty matrix). */
+/* What this thread's most recent successful glu_fwd / glu_bwd / glu_gemm_fwd
+ * enqueued.  `launched` is 0 when the call was a no-op (an empty matrix).
+ * For glu_gemm_fwd: path = 3, unroll = blocks per cluster (1, or 2 for a pair
+ * sharing each tile), vec_bytes = width of the y stores (16 or 2), grid =
+ * blocks of the persistent grid, vector_units = tiles of y, and threads as
+ * launched; the other fields are 0. */
 typedef struct {
     int32_t launched;     /* 1 if a kernel was enqueued */
     int32_t backward;     /* 0 = forward kernel, 1 = backward kernel */
@@ -243,7 +247,7 @@ typedef struct {
     int32_t threads;      /* threads per block */
     int32_t grid;         /* blocks launched */
     int32_t flattened;    /* 1 if the rows were contiguous and walked as one row */
-    int32_t path;         /* 1 = direct loads, 2 = bulk copies staged in shared memory */
+    int32_t path;         /* 1 = direct loads, 2 = bulk copies staged in shared memory, 3 = GEMM */
     int64_t vector_units; /* full-width accesses per operand */
     int64_t tail_elems;   /* elements handled one at a time (row ends) */
 } glu_launch_info_t;

@@ -88,8 +88,10 @@ def check_bound(orc, act, dt, y_bits, g, u, sg, su, K, what):
 
 # ---------------------------------------------------------------- exact grid inputs, every output
 
+# M <= 128 runs one block per tile, larger M pairs of blocks on 256 rows;
+# I <= 64 takes 64-wide column tiles, larger I 128-wide ones
 SHAPES = [(1, 8, 1), (128, 64, 128), (127, 72, 65), (300, 200, 300), (129, 1000, 40), (257, 328, 200),
-          (64, 4096, 64)]
+          (64, 4096, 64), (700, 256, 520)]
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -104,6 +106,19 @@ def test_grid_inputs_every_output(orc, shape, act, dt):
     y, _, _ = run_gemm(x, wg, wu, dt, act, K)
     ref = orc.gemm_glu(act, dt, x, wg, wu)
     compare(y, ref, dt, what=f"gemm {act} {dt} {shape}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_many_tiles_per_block(orc, dt):
+    """More tiles than resident blocks: each block (or pair) walks several
+    tiles, alternating its two tensor-memory accumulators."""
+    M, K, I = 1536, 64, 6144
+    rng = np.random.default_rng(17)
+    x = glu_synth.grid_bits(rng, (M, K), dt)
+    wg = glu_synth.grid_bits(rng, (I, K), dt)
+    wu = glu_synth.grid_bits(rng, (I, K), dt)
+    y, _, _ = run_gemm(x, wg, wu, dt, "gelu_erf", K)
+    compare(y, orc.gemm_glu("gelu_erf", dt, x, wg, wu), dt, what="many tiles")
 
 
 # ---------------------------------------------------------------- normal inputs, accumulation bound
