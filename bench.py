@@ -58,12 +58,15 @@ def config(extra=None):
     return c
 
 
+# the sources the streaming kernels and their launch plan are built from
+STREAMING_SOURCES = ("glu_api.cu", "glu_inst_bf16.cu", "glu_kernels.cuh", "glu_math.cuh", "glu_plan.h")
+
+
 def source_sha() -> str:
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in STREAMING_SOURCES:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -443,6 +446,94 @@ def run_table(args):
               flush=True)
 
 
+# ---------------------------------------------------------------- gate/up GEMM with the activation in the epilogue
+
+GM, GK, GI = 4096, 4096, 14336      # tokens, hidden size, intermediate size of one MLP layer
+
+
+def run_gemm(args):
+    """The gate/up projections with SwiGLU in the epilogue (glu_gemm_fwd) on one
+    MLP layer, against the unfused path it replaces: one cuBLAS GEMM into a
+    [gate | up] matrix, then glu_fwd over it.  Operands (x 32 MiB, weights
+    224 MiB) exceed L2.  Prints one JSON line (not the headline metric)."""
+    import torch
+    import glu_activation_mlps_gb300 as glu
+
+    glu.build()
+    L = glu.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev).manual_seed(7)
+    x = torch.randn(GM, GK, device=dev, generator=gen).to(torch.bfloat16)
+    w = (torch.randn(2 * GI, GK, device=dev, generator=gen) / GK ** 0.5).to(torch.bfloat16)
+    wg, wu = w[:GI], w[GI:]
+    y = torch.empty(GM, GI, device=dev, dtype=torch.bfloat16)
+    h = torch.empty(GM, 2 * GI, device=dev, dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    flops = 2 * GM * GK * 2 * GI
+
+    def fused():
+        st = L.glu_gemm_fwd(x.data_ptr(), GK, wg.data_ptr(), wu.data_ptr(), GK, y.data_ptr(), GI,
+                            GM, GK, GI, 0, 2, s)
+        if st:
+            raise glu.GluError(st, "glu_gemm_fwd")
+
+    def unfused():
+        torch.matmul(x, w.T, out=h)
+        st = L.glu_fwd(h.data_ptr(), 2 * GI, None, 0, y.data_ptr(), GI, GM, GI, 1, 0, 2, s)
+        if st:
+            raise glu.GluError(st, "glu_fwd")
+
+    def timed(fn, K, W, clocks=None):
+        for _ in range(W):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark(True)
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark(False)
+        return e0.elapsed_time(e1) / K
+
+    K, W = max(1, args.steps), max(3, args.warmup)
+    clocks = ClockSampler(gpu_selector(0))
+    clocks.start()
+    fused_ms = timed(fused, K, W, clocks)
+    clock_info = clocks.stop()
+    info = glu.glu_last_launch()
+    gemm_ms = timed(lambda: torch.matmul(x, w.T, out=h), K, W)
+    unfused_ms = timed(unfused, K, W)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    peak = float(peaks["bf16_tflops"])
+    tf = flops / (fused_ms * 1e-3) / 1e12
+    line = {
+        "metric": "gate/up projections with SwiGLU in the epilogue, TFLOP/s (bf16, M=4096 K=4096 I=14336)",
+        "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": round(fused_ms, 5), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "one MLP layer's gate/up projections: x 4096x4096, w_gate and w_up "
+                               "14336x4096 (N(0,1) and N(0,1/4096), bf16), y 4096x14336",
+                   "l2": "operands (256 MiB) exceed L2", "launch": info},
+        "roofline": {"bound": "tensor", "kernel": "glu_gemm_fwd", "achieved": round(tf, 1), "peak": peak,
+                     "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)",
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None,
+                     "algorithmic_flops": flops},
+        "comparison": {"fused_ms": round(fused_ms, 4),
+                       "cublas_gemm_ms": round(gemm_ms, 4),
+                       "cublas_gemm_tflops": round(flops / (gemm_ms * 1e-3) / 1e12, 1),
+                       "cublas_gemm_plus_glu_fwd_ms": round(unfused_ms, 4),
+                       "speedup_vs_unfused": round(unfused_ms / fused_ms, 4)},
+        "gpu_launches": K,
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- CPU oracle arms
 
 def oracle_rows(orc, d, r0, r1, threads):
@@ -513,6 +604,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=3.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--gemm", action="store_true",
+                    help="time glu_gemm_fwd on one MLP layer against cuBLAS + glu_fwd (one JSON line)")
     ap.add_argument("--table", action="store_true",
                     help="print a throughput table of every named workload instead of the JSON line")
     ap.add_argument("--path", default="default", choices=["default", "direct", "bulk"],
@@ -526,6 +619,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.gemm:
+        run_gemm(args)
+        return
     if args.table:
         run_table(args)
         return

@@ -15,7 +15,10 @@
 // of 2 BN tensor-memory columns per row; tensor memory holds two of them, so
 // the MMAs of the next tile run while warps 2-5 read the finished one with
 // tcgen05.ld (one row per thread), apply the same fp32 activation as the
-// streaming kernels, round once and store.
+// streaming kernels and round once.  Each warp stages 32 x 32 boxes of y in
+// shared memory (64-byte swizzle) and the tensor-memory accelerator stores
+// them, so y leaves in whole 128-byte lines; when y's rows are not 16-byte
+// multiples the warps store from registers instead.
 //
 // Two shapes:
 //   * one block per tile of 128 rows: the stage holds the x slice and the gate
@@ -53,6 +56,7 @@ constexpr int BK = 64;                   // K per stage: 64 x 2 bytes = one 128-
 constexpr int kThreads = 192;            // warp 0 loads, warp 1 issues MMAs, warps 2-5 store
 constexpr int kEpiWarps = 4;
 constexpr int kRingBytes = 192 * 1024;   // shared memory given to the stage ring
+constexpr int kYBox = 32;                // y leaves through 32 x 32 boxes (64-byte rows, 64-byte swizzle)
 constexpr long long kBudget = 2000000000LL;   // ~1 s at 2 GHz
 
 template <int BN, int CTAS>
@@ -66,7 +70,8 @@ struct Shape {
     static constexpr int kAccCols = 2 * BN;                           // [gate | up] of one tile
     static constexpr int kTmemCols = 2 * kAccCols;                    // two tiles in flight
     static constexpr int kBars = 2 * kStages + 2 + 2 + 1;             // full, empty, acc_full, acc_empty, done
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBars * 8 + 16;
+    static constexpr int kStageY = kEpiWarps * 2 * kYBox * kYBox * 2;  // two y boxes per epilogue warp
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStageY + kBars * 8 + 16;
     static_assert(CTAS == 1 || CTAS == 2, "one block or a pair");
     static_assert(BN % 32 == 0 && BN >= 32 && kMmaN <= 256, "one MMA covers N = 2 BN <= 256");
     static_assert(kTmemCols == 256 || kTmemCols == 512, "a power-of-two column count");
@@ -82,6 +87,7 @@ struct Params {
     int m_blocks, i_blocks; // row blocks of 128 * CTAS rows, column blocks of BN
     int group_m;            // row blocks per group of the tile order
     int vec_store;          // y rows and base 16-byte aligned
+    int tma_store;          // the same: y leaves through shared memory and the tensor-memory accelerator
 };
 
 static __device__ unsigned int g_gemm_timeouts;
@@ -260,6 +266,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "memory");
 }
 
+// A 32 x 32 box of y from shared memory (64-byte swizzle) to global memory;
+// the tensor-memory accelerator drops rows and columns outside y.
+__device__ __forceinline__ void tma_store(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Tile t of the grouped order: group_m row blocks side by side walk the column blocks.
 __device__ __forceinline__ void tile_origin(const Params &p, int t, int &mb, int &ib)
 {
@@ -274,7 +297,8 @@ __device__ __forceinline__ void tile_origin(const Params &p, int t, int &mb, int
 template <class Act, class T, int BN, int CTAS>
 __global__ void __launch_bounds__(kThreads, 1)
     glu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
-                    const __grid_constant__ CUtensorMap tm_wu, const Params p)
+                    const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_y,
+                    const Params p)
 {
     using S = Shape<BN, CTAS>;
     using Cd = Codec<T>;
@@ -284,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = saddr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);     // 1024-byte aligned ring
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ST * S::kStageBytes);
+    unsigned char *ystage = smem + ST * S::kStageBytes;                     // 1024-byte aligned
+    uint64_t *full = reinterpret_cast<uint64_t *>(ystage + S::kStageY);
     uint64_t *empty = full + ST;
     uint64_t *acc_full = empty + ST;            // [2]: MMAs of a tile done
     uint64_t *acc_empty = acc_full + 2;         // [2]: the epilogue (of both blocks) has read a tile
@@ -295,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = CTAS == 1 ? 0u : cluster_rank();
+    const uint32_t rank = CTAS == 1 ? 0u : cluster_rank();     // block of the pair
     const int cluster = blockIdx.x / CTAS, n_clusters = gridDim.x / CTAS;
     const int n_tiles = p.m_blocks * p.i_blocks;
 
@@ -304,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicAdd(&g_gemm_timeouts, 1u);
         *abort_flag = 1;
         if constexpr (CTAS == 2) {
-            const uint32_t peer = mapa(saddr(const_cast<int *>(abort_flag)), rank ^ 1u);
-            asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1) : "memory");
+            const uint32_t other = mapa(saddr(const_cast<int *>(abort_flag)), rank ^ 1u);
+            asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(other), "r"(1) : "memory");
         }
     };
 
@@ -429,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31, one row per thread
         const int q = warp & 3;
         const uint32_t lane_base = uint32_t(q * 32) << 16;
+        uint32_t n_boxes = 0;           // y boxes this warp has handed to the copy engine
         int lt = 0;
         for (int t = cluster; t < n_tiles; t += n_clusters, ++lt) {
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
@@ -461,6 +487,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             arrive_cluster(mapa(saddr(&acc_empty[ab]), 0));
                     }
                 }
+                if (p.tma_store) {
+                    uint32_t packed[32 / Cd::kPerWord];
+#pragma unroll
+                    for (int j = 0; j < 32; j += Cd::kPerWord) {
+                        float f[Cd::kPerWord];
+#pragma unroll
+                        for (int e = 0; e < Cd::kPerWord; ++e)
+                            f[e] = op_fwd<Act, false>(__uint_as_float(g[j + e]), __uint_as_float(u[j + e]));
+                        packed[j / Cd::kPerWord] = Cd::put(f);
+                    }
+                    // this warp's 32 rows x 32 columns: row `lane` is 64 bytes,
+                    // its 16-byte chunk c stored at chunk c ^ ((lane / 2) % 4)
+                    const uint32_t buf = saddr(ystage) + uint32_t(q * 2 + (n_boxes & 1)) * (kYBox * kYBox * 2);
+                    if (lane == 0 && n_boxes >= 2)      // the box stored from this buffer has been read
+                        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();
+                    const uint32_t row = buf + uint32_t(lane) * 64u, sw = (uint32_t(lane) >> 1) & 3u;
+#pragma unroll
+                    for (uint32_t c = 0; c < 4; ++c)
+                        st_shared16(row + ((c ^ sw) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                    packed[4 * c + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) tma_store(&tm_y, buf, i0 + c0, m - lane);
+                    ++n_boxes;
+                    continue;
+                }
                 if (m >= p.M) continue;
                 uint32_t packed[32 / Cd::kPerWord];
 #pragma unroll
@@ -490,6 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        // every box this warp stored has left shared memory and reached global memory
+        if (lane == 0 && n_boxes > 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -535,24 +591,23 @@ EncodeFn encode_fn()
 }
 
 // A rows x cols row-major matrix (row stride in bytes) as a 2-D tensor map
-// whose box is 64 columns by `box_rows` rows, 128-byte swizzle, zero fill
-// outside the matrix.
+// with a box of box_cols x box_rows; loads read zeros outside the matrix and
+// stores drop what falls outside it.
 bool make_map(CUtensorMap *m, bool bf16, const void *base, int64_t rows, int64_t cols, int64_t stride_bytes,
-              int box_rows)
+              int box_cols, int box_rows, CUtensorMapSwizzle swizzle)
 {
     EncodeFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
     const cuuint64_t strides[1] = {cuuint64_t(stride_bytes)};
-    const cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+    const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
 template <class T, int BN, int CTAS>
 KernelFn pick_act(int act)
@@ -569,25 +624,28 @@ KernelFn pick_act(int act)
 struct Variant {
     KernelFn fn;
     int smem;
+    int id;         // 0..3, see pick()
 };
 
 template <int BN, int CTAS>
-Variant variant(bool bf16, int act)
+Variant variant(bool bf16, int act, int id)
 {
     return {bf16 ? pick_act<__nv_bfloat16, BN, CTAS>(act) : pick_act<__half, BN, CTAS>(act),
-            Shape<BN, CTAS>::kSmemBytes};
+            Shape<BN, CTAS>::kSmemBytes, id};
 }
 
+// One block per 128-row tile while M fits one row block, pairs of blocks on
+// 256 rows beyond that; 64-wide column tiles when I fits one.
 Variant pick(bool bf16, int act, int bn, int ctas)
 {
-    if (bn == 64) return ctas == 1 ? variant<64, 1>(bf16, act) : variant<64, 2>(bf16, act);
-    return ctas == 1 ? variant<128, 1>(bf16, act) : variant<128, 2>(bf16, act);
+    if (ctas == 1) return bn == 64 ? variant<64, 1>(bf16, act, 0) : variant<128, 1>(bf16, act, 1);
+    return bn == 64 ? variant<64, 2>(bf16, act, 2) : variant<128, 2>(bf16, act, 3);
 }
 
 // Per kernel variant and device: the shared-memory opt-in done, and how many
 // blocks (one shape) or pairs (the other) fit on the GPU at once.
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_slots[kMaxDevices][2][4][2][2];
+std::atomic<int> g_slots[kMaxDevices][2][4][4];
 
 bool overlap(uintptr_t a0, uint64_t alen, uintptr_t b0, uint64_t blen)
 {
@@ -643,7 +701,7 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
 
     const bool bf16 = dtype == GLU_BF16;
     const int bn = I <= 64 ? 64 : 128;
-    const int ctas = M > BM ? 2 : 1;          // a pair of blocks per 256 rows once there are two row blocks
+    const int ctas = M > BM ? 2 : 1;
     const Variant v = pick(bf16, act, bn, ctas);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -662,33 +720,41 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     cfg.dynamicSmemBytes = size_t(v.smem);
     cfg.stream = s;
 
-    std::atomic<int> &slots = g_slots[dev % kMaxDevices][bf16][act][bn == 128][ctas == 2];
+    std::atomic<int> &slots = g_slots[dev % kMaxDevices][bf16][act][v.id];
     int n_slots = slots.load(std::memory_order_acquire);
     if (n_slots == 0) {
         e = cudaFuncSetAttribute(reinterpret_cast<const void *>(v.fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  v.smem);
         if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
         n_slots = sms;
-        if (ctas == 2) {
+        if (ctas > 1) {
             cudaLaunchConfig_t q = cfg;
-            q.gridDim = dim3(unsigned(sms - sms % 2));
+            q.gridDim = dim3(unsigned(sms - sms % ctas));
             q.attrs = &attr[1];
             q.numAttrs = 1;
             int clusters = 0;
             e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(v.fn), &q);
             if (e != cudaSuccess || clusters <= 0) {
                 (void)cudaGetLastError();
-                clusters = sms / 2;
+                clusters = sms / ctas;
             }
             n_slots = clusters;
         }
         slots.store(n_slots, std::memory_order_release);
     }
 
-    CUtensorMap tx, tg, tu;
-    if (!make_map(&tx, bf16, x, M, K, x_stride * E, BM) || !make_map(&tg, bf16, w_gate, I, K, w_stride * E, bn) ||
-        !make_map(&tu, bf16, w_up, I, K, w_stride * E, bn))
+    const bool y_aligned = (uintptr_t(y) % 16 == 0) && ((y_stride * E) % 16 == 0);
+    CUtensorMap tx, tg, tu, ty;
+    if (!make_map(&tx, bf16, x, M, K, x_stride * E, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tg, bf16, w_gate, I, K, w_stride * E, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tu, bf16, w_up, I, K, w_stride * E, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B))
         return glu::cuda_fail(cudaErrorInvalidValue);
+    // y through the copy engine when its rows allow, else direct stores (the map is then
+    // unused).  The engine clips a box at y's last column in 16-byte units, so the
+    // row width must be a whole number of them.
+    const bool y_map = y_aligned && (I * E) % 16 == 0 &&
+                       make_map(&ty, bf16, y, M, I, y_stride * E, kYBox, kYBox, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!y_map) ty = tx;
 
     Params p{};
     p.y = static_cast<char *>(y);
@@ -706,12 +772,13 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     int64_t group = (int64_t(48) << 20) / block_bytes;
     group = group < 1 ? 1 : (group > p.m_blocks ? p.m_blocks : group);
     p.group_m = int(group);
-    p.vec_store = (uintptr_t(y) % 16 == 0) && ((y_stride * E) % 16 == 0);
+    p.vec_store = y_aligned;
+    p.tma_store = y_map;
     const int64_t tiles = int64_t(p.m_blocks) * p.i_blocks;
     if (tiles * ctas > INT32_MAX) return GLU_ERR_SHAPE;
     const int64_t clusters = tiles < n_slots ? tiles : n_slots;     // persistent
 
-    void *args[] = {&tx, &tg, &tu, &p};
+    void *args[] = {&tx, &tg, &tu, &ty, &p};
     cfg.gridDim = dim3(unsigned(clusters * ctas));
     cfg.attrs = attr;
     cfg.numAttrs = 2;
@@ -725,7 +792,7 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
     glu_launch_info_t info{};
     info.launched = 1;
-    info.vec_bytes = p.vec_store ? 16 : E;
+    info.vec_bytes = p.tma_store ? 2 * kYBox : (p.vec_store ? 16 : E);
     info.unroll = ctas;
     info.threads = kThreads;
     info.grid = int32_t(clusters * ctas);

@@ -236,7 +236,10 @@ int glu_version(void);
 /* What this thread's most recent successful glu_fwd / glu_bwd / glu_gemm_fwd
  * enqueued.  `launched` is 0 when the call was a no-op (an empty matrix).
  * For glu_gemm_fwd: path = 3, unroll = blocks per cluster (1, or 2 for a pair
- * sharing each tile), vec_bytes = width of the y stores (16 or 2), grid =
+ * sharing each tile), vec_bytes = bytes per row of
+ * each y store (64: 32 x 32 boxes through the tensor-memory accelerator, used
+ * when y, its row stride and its row width are 16-byte multiples; else 16 or
+ * 2 from registers), grid =
  * blocks of the persistent grid, vector_units = tiles of y, and threads as
  * launched; the other fields are 0. */
 typedef struct {

@@ -89,9 +89,13 @@ def check_bound(orc, act, dt, y_bits, g, u, sg, su, K, what):
 # ---------------------------------------------------------------- exact grid inputs, every output
 
 # M <= 128 runs one block per tile, larger M pairs of blocks on 256 rows;
-# I <= 64 takes 64-wide column tiles, larger I 128-wide ones
+# I <= 64 takes 64-wide column tiles, larger I 128-wide ones.
 SHAPES = [(1, 8, 1), (128, 64, 128), (127, 72, 65), (300, 200, 300), (129, 1000, 40), (257, 328, 200),
-          (64, 4096, 64), (700, 256, 520)]
+          (64, 4096, 64), (700, 256, 520), (333, 136, 100)]
+
+
+def cluster_size(M, I):
+    return 1 if M <= 128 else 2
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -104,6 +108,8 @@ def test_grid_inputs_every_output(orc, shape, act, dt):
     wg = glu_synth.grid_bits(rng, (I, K), dt)
     wu = glu_synth.grid_bits(rng, (I, K), dt)
     y, _, _ = run_gemm(x, wg, wu, dt, act, K)
+    info = glu.glu_last_launch()
+    assert info["path"] == 3 and info["unroll"] == cluster_size(M, I) and info["grid"] % info["unroll"] == 0
     ref = orc.gemm_glu(act, dt, x, wg, wu)
     compare(y, ref, dt, what=f"gemm {act} {dt} {shape}")
 
@@ -137,25 +143,31 @@ def test_normal_inputs_accumulation_bound(orc, shape, act, dt):
 
 # ---------------------------------------------------------------- strides, padding, store paths
 
+@pytest.mark.parametrize("I,y_stride,y_offset,store", [(77, 82, 1, 2), (77, 88, 0, 16), (80, 88, 0, 64)],
+                         ids=["misaligned", "aligned-ragged-width", "aligned"])
 @pytest.mark.parametrize("dt", DTYPES)
-def test_padded_operands_and_misaligned_strided_output(orc, dt):
+def test_padded_operands_and_strided_output(orc, dt, I, y_stride, y_offset, store):
     """K = 20 is not a multiple of the 64-wide K slice nor of 8: the operands
     live in rows of 24 elements whose pad holds 1e4 (never read: the copy
-    engine zero-fills beyond K).  y starts one element past a 16-byte boundary
-    with a row stride of I + 5, and the words around it must stay untouched."""
-    M, K, I, S = 150, 20, 77, 24
+    engine zero-fills beyond K).  y has I columns in rows of y_stride: one
+    element past a 16-byte boundary (element stores), 16-byte aligned with a
+    width that is not (16-byte stores from registers), or aligned throughout
+    (boxes through the copy engine, clipped at column I and row M).  The words
+    around y must stay untouched."""
+    M, K, S = 150, 20, 24
     rng = np.random.default_rng(13)
     big = glu_synth.f32_to_bits(np.array([1e4], dtype=np.float32), dt)[0]
     x = glu_synth.grid_bits(rng, (M, K), dt)
     wg = glu_synth.grid_bits(rng, (I, K), dt)
     wu = glu_synth.grid_bits(rng, (I, K), dt)
     y, ybuf, ys = run_gemm(padded(x, S, big), padded(wg, S, big), padded(wu, S, big), dt, "silu", K,
-                           y_stride=I + 5, y_offset=1)
+                           y_stride=y_stride, y_offset=y_offset)
+    assert glu.glu_last_launch()["vec_bytes"] == store
     compare(y, orc.gemm_glu("silu", dt, x, wg, wu), dt, what="padded")
     # the gaps between y's rows and the words before and after it are still NaN
     inside = np.zeros(ybuf.size, dtype=bool)
     for m in range(M):
-        inside[1 + m * ys: 1 + m * ys + I] = True
+        inside[y_offset + m * ys: y_offset + m * ys + I] = True
     nan_bits = to_bits(torch.full((1,), float("nan"), dtype=TORCH[dt]), dt)[0]
     assert np.all(ybuf[~inside] == nan_bits)
 
