@@ -66,6 +66,8 @@ def lib():
             L.oracle_decode_vec.argtypes = [ci, vp, dp, i64]
             L.oracle_gemm_glu_at.argtypes = [ci, ci, vp, i64, vp, vp, i64, i64, vp, vp, i64, vp, dp, dp, dp, dp]
             L.oracle_gemm_glu_at.restype = None
+            L.oracle_add_rmsnorm.argtypes = [ci, vp, vp, vp, vp, vp, dp, dp, i64, i64, ctypes.c_double]
+            L.oracle_add_rmsnorm.restype = None
             L.oracle_sigmoid.argtypes = [ctypes.c_double]
             L.oracle_sigmoid.restype = ctypes.c_double
             for f in (L.oracle_fwd, L.oracle_bwd, L.oracle_bwd_da_scale, L.oracle_act_vec,
@@ -258,3 +260,22 @@ def gemm_glu(act_name: str, dtype: str, x, w_gate, w_up):
     mm, ii = np.meshgrid(np.arange(M), np.arange(I), indexing="ij")
     y, *_ = gemm_glu_at(act_name, dtype, x, w_gate, w_up, mm.ravel(), ii.ravel())
     return y.reshape(M, I)
+
+
+# ---- fused residual add + RMSNorm --------------------------------------------
+
+def add_rmsnorm(dtype: str, x, res, gamma, eps: float):
+    """h = x + res (exact, stored rounded), y = round(h * rstd * gamma) with
+    rstd = 1 / sqrt(mean(h^2) + eps) over each row of the exact h.  x and res
+    are (rows, H) bit arrays, gamma (H,).  Returns (h, y, rstd, y_exact)."""
+    x, res = _bits(x, dtype), _bits(res, dtype)
+    gamma = _bits(gamma, dtype)
+    if x.ndim != 2 or res.shape != x.shape or gamma.shape != (x.shape[1],):
+        raise ValueError("x and res are (rows, H), gamma is (H,)")
+    rows, H = x.shape
+    h, y = np.empty_like(x), np.empty_like(x)
+    rstd = np.empty(rows)
+    y_exact = np.empty((rows, H))
+    lib().oracle_add_rmsnorm(DTYPES[dtype], _ptr(x), _ptr(res), _ptr(gamma), _ptr(h), _ptr(y), _ptr(rstd),
+                             _ptr(y_exact), rows, H, float(eps))
+    return h, y, rstd, y_exact

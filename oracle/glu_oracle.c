@@ -22,9 +22,16 @@
  *
  * Nothing here is blocked, fused or reordered: each output element is the
  * plain formula applied to the corresponding input elements.
+ *
+ * Two further operations of the same MLP block, each the plain definition
+ * written out: the gate/up projections with the activation applied (dot
+ * products in double, k in order) and the fused residual add + RMSNorm of
+ * "Skill: Write a Triton Fused Add+RMSNorm Kernel" (row sums of squares in
+ * double, compensated).
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* enum values are part of the oracle's own calling convention */
@@ -341,4 +348,55 @@ void oracle_gemm_glu_at(int act, int dtype, const void *x, int64_t sx, const voi
         if (sg) sg[j] = ag;
         if (su) su[j] = au;
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* Fused residual add + RMSNorm ("Skill: Write a Triton Fused Add+RMSNorm
+ * Kernel": Purpose, y = rmsnorm(x + residual) with x + residual written back;
+ * Required reasoning process steps 3-7; Kernel design rules, eps inside the
+ * square root, gamma indexed by column only, no mean and no bias):
+ *   h[j]  = x[j] + res[j]                   exact; the stored h is rounded once
+ *   ms    = (1/H) * sum_j h[j]^2            of the exact h, over the whole row
+ *   rstd  = 1 / sqrt(ms + eps)
+ *   y[j]  = round(h[j] * rstd * gamma[j])
+ * All rows contiguous (row r starts at r * H); gamma has H entries in the
+ * input dtype.  The sum of squares is compensated (Neumaier), so its relative
+ * error stays near 2^-53 for any H.  Outputs: h and y as bit patterns, rstd
+ * per row and the unrounded y (both in double; either pointer may be NULL). */
+static double row_sum_squares(const double *h, int64_t H)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t j = 0; j < H; ++j) {
+        const double t = h[j] * h[j];
+        const double u = s + t;
+        if (fabs(s) >= fabs(t))
+            c += (s - u) + t;
+        else
+            c += (t - u) + s;
+        s = u;
+    }
+    return s + c;
+}
+
+void oracle_add_rmsnorm(int dtype, const void *x, const void *res, const void *gamma, void *h, void *y,
+                        double *rstd, double *y_exact, int64_t n_rows, int64_t H, double eps)
+{
+    double *hv = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int64_t j = 0; j < H; ++j) {
+            const int64_t i = r * H + j;
+            hv[j] = oracle_decode(load_bits(x, i, dtype), dtype) + oracle_decode(load_bits(res, i, dtype), dtype);
+            store_bits(h, i, dtype, oracle_encode(hv[j], dtype));
+        }
+        const double ms = row_sum_squares(hv, H) / (double)H;
+        const double rs = 1.0 / sqrt(ms + eps);
+        if (rstd) rstd[r] = rs;
+        for (int64_t j = 0; j < H; ++j) {
+            const int64_t i = r * H + j;
+            const double v = hv[j] * rs * oracle_decode(load_bits(gamma, j, dtype), dtype);
+            store_bits(y, i, dtype, oracle_encode(v, dtype));
+            if (y_exact) y_exact[i] = v;
+        }
+    }
+    free(hv);
 }

@@ -420,3 +420,120 @@ def test_gemm_glu_exact_integer_case(orc):
     assert g[0] == 4.0 and u[0] == 4.0 and orc.decode("bf16", y)[0] == 16.0
     y2 = orc.gemm_glu("gelu_tanh", "bf16", x, wg, wu)
     assert orc.decode("bf16", y2)[0, 0] == orc.round_to("bf16", orc.act("gelu_tanh", [4.0]) * 4.0)[0]
+
+
+# --------------------------------------------------------------------------- residual add + RMSNorm
+# Page: "Skill: Write a Triton Fused Add+RMSNorm Kernel" (AR).
+
+def _bf16(v):
+    return glu_synth.f32_to_bits(np.asarray(v, dtype=np.float32), "bf16")
+
+
+def test_add_rmsnorm_constant_row_closed_form(orc):
+    """A constant row h = c: mean square c^2, so rstd = 1/sqrt(c^2 + eps) and
+    y = c * rstd * gamma.  With eps = 1 the eps-inside-the-root form of (AR)
+    Kernel design rules (1.75/sqrt(1.75^2 + 1) = 0.868) differs from eps outside
+    (1.75/2.75) and from a mean-subtracting norm (0)."""
+    H = 6
+    x = _bf16(np.full((1, H), 1.5))
+    r = _bf16(np.full((1, H), 0.25))
+    g = _bf16(np.full(H, 2.0))
+    h, y, rstd, ye = orc.add_rmsnorm("bf16", x, r, g, 1.0)
+    want = 1.0 / math.sqrt(1.75 ** 2 + 1.0)
+    assert rstd[0] == pytest.approx(want, rel=1e-15)
+    assert np.allclose(ye, 1.75 * want * 2.0, rtol=1e-15, atol=0)
+    assert np.all(orc.decode("bf16", h) == 1.75)
+
+
+def test_add_rmsnorm_unit_rms_identity(orc):
+    """rstd^2 * mean(h^2) + eps * rstd^2 = 1, i.e. mean((y/gamma)^2) + eps*rstd^2 = 1
+    for every row: fixes the denominator H and the placement of eps."""
+    rng = np.random.default_rng(50)
+    rows, H = 5, 777
+    x = glu_synth.normal_bits(rng, (rows, H), 1.0, "bf16")
+    r = glu_synth.normal_bits(rng, (rows, H), 3.0, "bf16")
+    g = glu_synth.normal_bits(rng, H, 1.0, "bf16")
+    gv = orc.decode("bf16", g)
+    for eps in (1e-6, 0.5, 7.0):
+        _, _, rstd, ye = orc.add_rmsnorm("bf16", x, r, g, eps)
+        lhs = np.mean((ye / gv) ** 2, axis=1) + eps * rstd ** 2
+        assert np.allclose(lhs, 1.0, rtol=0, atol=1e-13)
+
+
+def test_add_rmsnorm_gamma_is_per_column(orc):
+    """y[r, j] / (h[r, j] * gamma[j]) is the same rstd[r] for every column j of
+    every row ((AR) step 6: gamma indexed by the column only)."""
+    rng = np.random.default_rng(51)
+    rows, H = 4, 64
+    x = glu_synth.normal_bits(rng, (rows, H), 1.0, "f16")
+    r = glu_synth.normal_bits(rng, (rows, H), 1.0, "f16")
+    g = glu_synth.f32_to_bits(np.linspace(0.5, 3.0, H, dtype=np.float32), "f16")
+    _, _, rstd, ye = orc.add_rmsnorm("f16", x, r, g, 1e-5)
+    h = orc.decode("f16", x) + orc.decode("f16", r)
+    ratio = ye / (h * orc.decode("f16", g)[None, :])
+    assert np.allclose(ratio, rstd[:, None], rtol=1e-14, atol=0)
+    assert len(set(np.round(rstd, 12))) == rows
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_add_rmsnorm_stored_sum_is_the_rounded_sum(orc, dt):
+    """The stored h is x + res rounded once ((AR) step 4): checked against
+    numpy's float16/float32 and torch's bfloat16 conversion of the float64 sum."""
+    rng = np.random.default_rng(52)
+    x = glu_synth.normal_bits(rng, (3, 500), 1.0, dt)
+    r = glu_synth.normal_bits(rng, (3, 500), 50.0, dt)
+    g = glu_synth.normal_bits(rng, 500, 1.0, dt)
+    h, *_ = orc.add_rmsnorm(dt, x, r, g, 1e-6)
+    s = orc.decode(dt, x) + orc.decode(dt, r)
+    if dt == "f16":
+        want = s.astype(np.float16).view(np.uint16)
+    elif dt == "f32":
+        want = s.astype(np.float32).view(np.uint32)
+    else:
+        want = torch.from_numpy(s).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(h, want)
+
+
+def test_add_rmsnorm_squares_the_exact_sum(orc):
+    """(AR) step 3: the add runs before any narrowing.  x = (1, 1), res = (2^-9, 0)
+    in bf16: the exact h = (1 + 2^-9, 1) is not a bf16 pair (the stored h is
+    (1, 1)), and the mean square is that of the exact h."""
+    x = _bf16([[1.0, 1.0]])
+    r = _bf16([[2.0 ** -9, 0.0]])
+    g = _bf16([1.0, 1.0])
+    eps = 1e-6
+    h, _, rstd, ye = orc.add_rmsnorm("bf16", x, r, g, eps)
+    assert np.all(orc.decode("bf16", h) == 1.0)
+    ms = ((1 + 2.0 ** -9) ** 2 + 1.0) / 2
+    assert rstd[0] == pytest.approx(1 / math.sqrt(ms + eps), rel=1e-15)
+    assert ye[0, 1] == pytest.approx(1 / math.sqrt(ms + eps), rel=1e-15)
+    assert ye[0, 1] != pytest.approx(1 / math.sqrt(1.0 + eps), rel=1e-8)
+
+
+def test_add_rmsnorm_matches_torch_rms_norm(orc):
+    """torch.nn.functional.rms_norm in float64 on x + res with weight gamma."""
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    rng = np.random.default_rng(53)
+    rows, H = 6, 4096
+    x = glu_synth.normal_bits(rng, (rows, H), 1.0, "bf16")
+    r = glu_synth.normal_bits(rng, (rows, H), 2.0, "bf16")
+    g = glu_synth.normal_bits(rng, H, 0.3, "bf16")
+    _, y, _, ye = orc.add_rmsnorm("bf16", x, r, g, 1e-5)
+    h = torch.from_numpy(orc.decode("bf16", x) + orc.decode("bf16", r))
+    want = F.rms_norm(h, (H,), weight=torch.from_numpy(orc.decode("bf16", g)), eps=1e-5).numpy()
+    assert np.allclose(ye, want, rtol=1e-12, atol=1e-300)
+    assert np.array_equal(orc.decode("bf16", y), orc.round_to("bf16", want))
+
+
+def test_add_rmsnorm_scale_invariance(orc):
+    """Scaling x and res by 2^k and eps by 4^k leaves y unchanged (exact in bf16)."""
+    rng = np.random.default_rng(54)
+    x = glu_synth.normal_bits(rng, (3, 300), 1.0, "bf16")
+    r = glu_synth.normal_bits(rng, (3, 300), 1.0, "bf16")
+    g = glu_synth.normal_bits(rng, 300, 1.0, "bf16")
+    _, _, _, ye = orc.add_rmsnorm("bf16", x, r, g, 1e-3)
+    xs = _bf16(orc.decode("bf16", x) * 2.0 ** 40)
+    rs = _bf16(orc.decode("bf16", r) * 2.0 ** 40)
+    _, _, _, ye2 = orc.add_rmsnorm("bf16", xs, rs, g, 1e-3 * 2.0 ** 80)
+    assert np.allclose(ye, ye2, rtol=1e-14, atol=0)
