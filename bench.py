@@ -534,6 +534,103 @@ def run_gemm(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- residual add + RMSNorm
+
+def run_rmsnorm(args):
+    """glu_add_rmsnorm_fwd on one decoder block's residual add + RMSNorm (4096
+    tokens x hidden 4096, bf16, eps 1e-5, rstd kept), and an H sweep, against
+    torch's unfused path (an add kernel, then F.rms_norm).  Each timed launch
+    uses the next of several buffer sets whose total exceeds L2.  Prints one
+    JSON line (not the headline metric)."""
+    import torch
+    import torch.nn.functional as F
+    import glu_activation_mlps_gb300 as glu
+
+    glu.build()
+    L = glu.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    gen = torch.Generator(device=dev).manual_seed(8)
+    peak, peak_src = measured_peak()
+    K, W = max(1, args.steps), max(3, args.warmup)
+
+    def timed(fn, nsets, clocks=None):
+        for k in range(W):
+            fn(k % nsets)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark(True)
+        e0.record(stream)
+        for k in range(K):
+            fn(k % nsets)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark(False)
+        return e0.elapsed_time(e1) / K
+
+    def case(rows, H, clocks=None):
+        E = 2
+        per_set = 4 * rows * H * E
+        nsets = max(2, -(-3 * L2_BYTES // per_set))
+        sets = []
+        for _ in range(nsets):
+            x = torch.randn(rows, H, device=dev, generator=gen).to(torch.bfloat16)
+            r = (torch.randn(rows, H, device=dev, generator=gen) * 4).to(torch.bfloat16)
+            sets.append((x, r, torch.empty_like(x), torch.empty_like(x)))
+        g = (1 + 0.1 * torch.randn(H, device=dev, generator=gen)).to(torch.bfloat16)
+        rstd = torch.empty(rows, device=dev, dtype=torch.float32)
+
+        def fused(k):
+            x, r, h, y = sets[k]
+            st = L.glu_add_rmsnorm_fwd(x.data_ptr(), H, r.data_ptr(), H, g.data_ptr(), h.data_ptr(), H,
+                                       y.data_ptr(), H, rstd.data_ptr(), rows, H, 1e-5, 2, s)
+            if st:
+                raise glu.GluError(st, "glu_add_rmsnorm_fwd")
+
+        def unfused(k):
+            x, r, h, y = sets[k]
+            torch.add(x, r, out=h)
+            y.copy_(F.rms_norm(h, (H,), g, 1e-5))
+
+        ms = timed(fused, nsets, clocks)
+        info = glu.glu_last_launch()
+        ms_unfused = timed(unfused, nsets)
+        nbytes = 4 * rows * H * E + H * E + 4 * rows
+        return {"rows": rows, "H": H, "ms": round(ms, 5), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "torch_unfused_ms": round(ms_unfused, 5),
+                "speedup_vs_unfused": round(ms_unfused / ms, 3), "bytes": nbytes, "launch": info,
+                "buffer_sets": nsets}
+
+    clocks = ClockSampler(gpu_selector(0))
+    clocks.start()
+    main = case(4096, 4096, clocks)
+    clock_info = clocks.stop()
+    sweep = [case(4096, H) for H in (1024, 2048, 8192, 16384)]
+    line = {
+        "metric": "fused residual add + RMSNorm achieved HBM GB/s (bf16, 4096 tokens x hidden 4096)",
+        "value": main["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": main["ms"], "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "h = x + residual, y = rmsnorm(h) * gamma, eps 1e-5, rstd kept; x ~ N(0,1), "
+                               "residual ~ N(0,4^2), gamma ~ 1 + N(0,0.1^2)",
+                   "l2": f"each launch uses the next of {main['buffer_sets']} buffer sets (together > L2)",
+                   "launch": main["launch"]},
+        "roofline": {"bound": "hbm", "kernel": "glu_add_rmsnorm_fwd", "achieved": main["gbs"], "peak": peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy)", "unit": "GB/s",
+                     "frac": main["frac"], "traffic": None, "algorithmic_bytes": main["bytes"]},
+        "comparison": {"torch_add_then_rms_norm_ms": main["torch_unfused_ms"],
+                       "speedup_vs_unfused": main["speedup_vs_unfused"]},
+        "sweep": [{k: c[k] for k in ("rows", "H", "ms", "gbs", "frac", "torch_unfused_ms", "speedup_vs_unfused")}
+                  for c in sweep],
+        "gpu_launches": K,
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- CPU oracle arms
 
 def oracle_rows(orc, d, r0, r1, threads):
@@ -606,6 +703,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--gemm", action="store_true",
                     help="time glu_gemm_fwd on one MLP layer against cuBLAS + glu_fwd (one JSON line)")
+    ap.add_argument("--rmsnorm", action="store_true",
+                    help="time glu_add_rmsnorm_fwd on one decoder block against torch's add + rms_norm")
     ap.add_argument("--table", action="store_true",
                     help="print a throughput table of every named workload instead of the JSON line")
     ap.add_argument("--path", default="default", choices=["default", "direct", "bulk"],
@@ -621,6 +720,9 @@ def main():
 
     if args.gemm:
         run_gemm(args)
+        return
+    if args.rmsnorm:
+        run_rmsnorm(args)
         return
     if args.table:
         run_table(args)

@@ -25,13 +25,15 @@ ACT = {"silu": 0, "gelu_erf": 1, "gelu_tanh": 2, "relu": 3}
 LAYOUT = {"split": 0, "concat": 1}
 DTYPE = {"f32": 0, "f16": 1, "bf16": 2}
 STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STRIDE",
-          -4: "GLU_ERR_ALIAS", -5: "GLU_ERR_ENUM", -6: "GLU_ERR_CUDA", -7: "GLU_ERR_WORKSPACE"}
+          -4: "GLU_ERR_ALIAS", -5: "GLU_ERR_ENUM", -6: "GLU_ERR_CUDA", -7: "GLU_ERR_WORKSPACE",
+          -8: "GLU_ERR_VALUE"}
 
 # Every symbol include/glu.h declares.
 EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_fwd_host_noalloc",
            "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
-           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_gemm_fwd")
+           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_gemm_fwd",
+           "glu_add_rmsnorm_fwd")
 
 
 class GluError(RuntimeError):
@@ -107,6 +109,9 @@ def lib() -> ctypes.CDLL:
             L.glu_wait_timeouts.restype = ci
             L.glu_gemm_fwd.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, i64, ci, ci, vp]
             L.glu_gemm_fwd.restype = ci
+            L.glu_add_rmsnorm_fwd.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i64, vp, i64, i64,
+                                              ctypes.c_float, ci, vp]
+            L.glu_add_rmsnorm_fwd.restype = ci
             _lib = L
     return _lib
 
@@ -187,6 +192,12 @@ def glu_wait_timeouts(reset: bool = False) -> int:
 
 def glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream) -> int:
     return lib().glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream)
+
+
+def glu_add_rmsnorm_fwd(x, x_stride, residual, res_stride, gamma, h, h_stride, y, y_stride, rstd,
+                        n_rows, n_cols, eps, dtype, stream) -> int:
+    return lib().glu_add_rmsnorm_fwd(x, x_stride, residual, res_stride, gamma, h, h_stride, y, y_stride, rstd,
+                                     n_rows, n_cols, eps, dtype, stream)
 
 
 def glu_get_tuning() -> dict:
@@ -336,6 +347,40 @@ def gemm_fwd(x, w_gate, w_up, *, y=None, act: str = "silu", stream=None):
     if st:
         raise GluError(st, "glu_gemm_fwd")
     return y
+
+
+def add_rmsnorm(x, residual, gamma, eps: float = 1e-5, *, h=None, y=None, rstd=None, stream=None):
+    """h = x + residual and y = rmsnorm(h) * gamma over the last dimension, in one
+    pass.  ``h`` and ``y`` may be given (h may be x or residual for an in-place
+    residual update, y the other one); ``rstd`` may be a float32 tensor of one
+    entry per row, or True to allocate it.  Returns (h, y) or (h, y, rstd)."""
+    import torch
+    n_rows, x_stride = _rows(x, "x")
+    _, r_stride = _rows(residual, "residual")
+    if residual.shape != x.shape or residual.dtype != x.dtype:
+        raise ValueError("residual must match x in shape and dtype")
+    H = x.shape[-1]
+    if gamma.shape != (H,) or gamma.dtype != x.dtype or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous (H,) tensor of x's dtype")
+    h = torch.empty_like(x) if h is None else h
+    y = torch.empty_like(x) if y is None else y
+    for t, n in ((h, "h"), (y, "y")):
+        if t.shape != x.shape or t.dtype != x.dtype:
+            raise ValueError(f"{n} must match x in shape and dtype")
+    _, h_stride = _rows(h, "h")
+    _, y_stride = _rows(y, "y")
+    want_rstd = rstd is not None and rstd is not False
+    if rstd is True:
+        rstd = torch.empty(n_rows, dtype=torch.float32, device=x.device)
+    if want_rstd and (rstd.dtype != torch.float32 or rstd.numel() != n_rows or not rstd.is_contiguous()):
+        raise ValueError("rstd must be a contiguous float32 tensor with one entry per row")
+    st = glu_add_rmsnorm_fwd(x.data_ptr(), x_stride, residual.data_ptr(), r_stride, gamma.data_ptr(),
+                             h.data_ptr(), h_stride, y.data_ptr(), y_stride,
+                             rstd.data_ptr() if want_rstd else None, n_rows, H, float(eps),
+                             _dtype_code(x), _stream(stream))
+    if st:
+        raise GluError(st, "glu_add_rmsnorm_fwd")
+    return (h, y, rstd) if want_rstd else (h, y)
 
 
 # ---- host tensors ---------------------------------------------------------------

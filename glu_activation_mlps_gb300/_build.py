@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libglu_gb300.so")
 
 SOURCES = ["glu_api.cu", "glu_host.cu", "glu_noalloc.cu", "glu_bulk.cu", "glu_inst_bf16.cu",
-           "glu_inst_f16.cu", "glu_inst_f32.cu", "glu_gemm.cu"]
+           "glu_inst_f16.cu", "glu_inst_f32.cu", "glu_gemm.cu", "glu_rmsnorm.cu"]
 HEADERS = ["glu_plan.h", "glu_math.cuh", "glu_kernels.cuh", "glu_bulk.cuh"]
 
 NVCC_FLAGS = [

@@ -99,6 +99,19 @@ bool elems_overlap(const Mat &X, const Mat &Y, int64_t rows, int E)
     return false;
 }
 
+// Does any of the rows of M (each width * E bytes) share a byte with [p, p + len)?
+bool rows_hit_range(const Mat &M, int64_t rows, int E, uint64_t p, uint64_t len)
+{
+    const uint64_t m0 = M.p, m1 = M.p + uint64_t(extent_bytes(M, rows, E));
+    if (m1 <= p || p + len <= m0) return false;
+    if (rows == 1) return true;
+    const uint64_t pitch = uint64_t(M.stride) * E, w = uint64_t(M.width) * E;
+    const uint64_t first = p > m0 ? (p - m0) / pitch : 0;      // the row at or before p
+    for (uint64_t r = first; r < uint64_t(rows) && m0 + r * pitch < p + len; ++r)
+        if (m0 + r * pitch + w > p) return true;
+    return false;
+}
+
 bool same_mat(const Mat &X, const Mat &Y, int64_t rows)
 {
     return X.p == Y.p && (rows == 1 || X.stride == Y.stride) && X.width == Y.width;
@@ -406,6 +419,44 @@ int validate_fwd(const void *a, int64_t a_stride, const void *b, int64_t b_strid
     return GLU_OK;
 }
 
+int validate_add_rmsnorm(const void *x, int64_t x_stride, const void *res, int64_t res_stride,
+                         const void *gamma, const void *h, int64_t h_stride, const void *y, int64_t y_stride,
+                         const float *rstd, int64_t n_rows, int64_t n_cols, float eps, int dtype, bool *empty)
+{
+    *empty = false;
+    if (!(dtype == GLU_F32 || dtype == GLU_F16 || dtype == GLU_BF16)) return GLU_ERR_ENUM;
+    if (n_rows < 0 || n_cols < 0) return GLU_ERR_SHAPE;
+    if (!(eps > 0.0f) || !(eps < INFINITY)) return GLU_ERR_VALUE;
+    if (n_rows == 0 || n_cols == 0) { *empty = true; return GLU_OK; }
+    if (n_cols > kRmsMaxCols) return GLU_ERR_SHAPE;
+    if (!x || !res || !gamma || !h || !y) return GLU_ERR_NULL;
+    if (n_rows == 1) x_stride = res_stride = h_stride = y_stride = n_cols;
+    if (x_stride < n_cols || res_stride < n_cols || h_stride < n_cols || y_stride < n_cols)
+        return GLU_ERR_STRIDE;
+    const int E = elem_size(dtype);
+    const Mat mx{uintptr_t(x), x_stride, n_cols}, mr{uintptr_t(res), res_stride, n_cols};
+    const Mat mh{uintptr_t(h), h_stride, n_cols}, my{uintptr_t(y), y_stride, n_cols};
+    const Mat mg{uintptr_t(gamma), n_cols, n_cols};
+    if (extent_bytes(mx, n_rows, E) < 0 || extent_bytes(mr, n_rows, E) < 0 || extent_bytes(mh, n_rows, E) < 0 ||
+        extent_bytes(my, n_rows, E) < 0 || extent_bytes(mg, 1, E) < 0)
+        return GLU_ERR_SHAPE;
+    const Mat ins[2] = {mx, mr}, outs[2] = {mh, my};
+    if (int st = check_aliasing(ins, 2, outs, 2, n_rows, E)) return st;
+    // gamma is read by every row: no output element may lie on it
+    for (const Mat &o : outs)
+        if (rows_hit_range(o, n_rows, E, mg.p, uint64_t(n_cols) * E)) return GLU_ERR_ALIAS;
+    if (rstd) {
+        if (uint64_t(n_rows) > (UINTPTR_MAX - uintptr_t(rstd)) / 4) return GLU_ERR_SHAPE;
+        const uint64_t r0 = uintptr_t(rstd), r1 = r0 + uint64_t(n_rows) * 4;
+        const Mat all[5] = {mx, mr, mh, my, mg};
+        for (int k = 0; k < 5; ++k) {
+            const uint64_t a0 = all[k].p, a1 = a0 + uint64_t(extent_bytes(all[k], k == 4 ? 1 : n_rows, E));
+            if (!(a1 <= r0 || r1 <= a0)) return GLU_ERR_ALIAS;
+        }
+    }
+    return GLU_OK;
+}
+
 int validate_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
                  int64_t b_stride, const void *da, int64_t da_stride, const void *db,
                  int64_t db_stride, int64_t n_rows, int64_t n_cols, int layout, int act, int dtype,
@@ -505,6 +556,7 @@ const char *glu_status_string(int status)
     case GLU_ERR_ENUM: return "unknown activation, layout, dtype or tuning value";
     case GLU_ERR_CUDA: return "the CUDA runtime refused a launch or copy";
     case GLU_ERR_WORKSPACE: return "the workspace is NULL or too small for one row";
+    case GLU_ERR_VALUE: return "a numeric argument is out of range (eps must be finite and > 0)";
     default: return "unknown status";
     }
 }

@@ -89,6 +89,12 @@ cudaError_t timeouts(unsigned int *count, bool reset);   // glu_gemm.cu
 }
 void record_launch(const glu_launch_info_t &info);       // this thread's glu_last_launch
 
+// Fused residual add + RMSNorm (glu_rmsnorm.cu): argument rules shared with glu_api.cu.
+constexpr int64_t kRmsMaxCols = 32768;
+int validate_add_rmsnorm(const void *x, int64_t x_stride, const void *res, int64_t res_stride,
+                         const void *gamma, const void *h, int64_t h_stride, const void *y, int64_t y_stride,
+                         const float *rstd, int64_t n_rows, int64_t n_cols, float eps, int dtype, bool *empty);
+
 // One validated call: what the planner needs.  Strides are in elements.
 struct Call {
     int dir, act, dtype, E;

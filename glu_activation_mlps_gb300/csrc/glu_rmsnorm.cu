@@ -1,0 +1,288 @@
+// Fused residual add + RMSNorm ("Skill: Write a Triton Fused Add+RMSNorm
+// Kernel": Purpose; Required reasoning process steps 1-9; Kernel design rules;
+// Correctness requirements):
+//
+//     s = x + residual (fp32),  h = round(s),
+//     rstd = 1 / sqrt(sum(s^2) / H + eps),  y = round(s * rstd * gamma)
+//
+// One block per row (more rows than blocks: the grid walks them).  Each thread
+// keeps EPT elements of s in fp32 registers, so x and the residual are read
+// once and h and y written once: 4 row passes of HBM traffic plus gamma, which
+// stays in L2 ("Performance requirements": the single-pass case).  Every
+// element is loaded and stored by one thread, its loads before its stores, and
+// y is stored only after the whole block has loaded its row, which makes h or
+// y written over x or the residual safe.  The sum of squares is compensated
+// within each thread, then reduced over the warp and the block in fp32; rstd
+// uses IEEE division and square root.
+//
+// Rows whose operands are 16-byte aligned (bases, strides and row width) use
+// 16-byte accesses, element i of a thread's k-th vector at column
+// (t + k * threads) * V + i; other rows use element accesses at column
+// t + k * threads.  Either way consecutive threads touch consecutive addresses.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "glu.h"
+#include "glu_kernels.cuh"
+#include "glu_plan.h"
+
+namespace glu {
+namespace rms {
+
+struct Params {
+    const char *x, *res, *gamma;
+    char *h, *y;
+    float *rstd;
+    int64_t sx, sr, sh, sy;     // row strides in bytes
+    int64_t rows;
+    int H;
+    float eps;
+};
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Sum of v over the block; every thread gets the result.  `red` holds 33 floats.
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float w = lane < nw ? red[lane] : 0.0f;
+        w = warp_sum(w);
+        if (lane == 0) red[32] = w;
+    }
+    __syncthreads();
+    const float r = red[32];
+    __syncthreads();            // red is reused by the next row
+    return r;
+}
+
+// Compensated accumulation (Neumaier): s + c carries the running sum.
+__device__ __forceinline__ void acc2(float &s, float &c, float t)
+{
+    const float u = s + t;
+    c += fabsf(s) >= fabsf(t) ? (s - u) + t : (t - u) + s;
+    s = u;
+}
+
+template <class T, int EPT, bool VEC>
+__global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
+    add_rmsnorm_kernel(const Params p)
+{
+    using C = Codec<T>;
+    constexpr int V = VEC ? 16 / int(sizeof(T)) : 1;      // elements per access
+    constexpr int NV = EPT / V;                           // accesses per thread per operand
+    constexpr int W = V / C::kPerWord > 0 ? V / C::kPerWord : 1;   // 32-bit words per access
+    __shared__ float red[33];
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const int t = threadIdx.x, nt = blockDim.x;
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const char *xr = p.x + row * p.sx, *rr = p.res + row * p.sr;
+        char *hr = p.h + row * p.sh, *yr = p.y + row * p.sy;
+        float s[EPT];
+        float ss = 0.0f, sc = 0.0f;
+        // loads go out in chunks of CK accesses per operand, all of a chunk's
+        // loads before its stores (each element is loaded and stored by this
+        // thread alone, so h over x or the residual stays correct)
+        if constexpr (VEC) {
+            constexpr int CK = NV < 4 ? NV : 4;
+#pragma unroll
+            for (int k0 = 0; k0 < NV; k0 += CK) {
+                uint32_t wx[CK][W], wr[CK][W];
+#pragma unroll
+                for (int k = 0; k < CK; ++k) {
+                    const int col = (t + (k0 + k) * nt) * V;
+                    if (col < p.H) {
+                        Access<16>::load(xr + int64_t(col) * sizeof(T), reinterpret_cast<uint32_t(&)[4]>(wx[k]));
+                        Access<16>::load(rr + int64_t(col) * sizeof(T), reinterpret_cast<uint32_t(&)[4]>(wr[k]));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < CK; ++k) {
+                    const int col = (t + (k0 + k) * nt) * V;
+                    float *sv = s + (k0 + k) * V;
+                    if (col < p.H) {
+                        uint32_t wh[W];
+#pragma unroll
+                        for (int j = 0; j < W; ++j) {
+                            float f[C::kPerWord];
+#pragma unroll
+                            for (int e = 0; e < C::kPerWord; ++e) {
+                                f[e] = C::get(wx[k][j], e) + C::get(wr[k][j], e);
+                                sv[j * C::kPerWord + e] = f[e];
+                                acc2(ss, sc, f[e] * f[e]);
+                            }
+                            wh[j] = C::put(f);
+                        }
+                        Access<16>::store(hr + int64_t(col) * sizeof(T), reinterpret_cast<const uint32_t(&)[4]>(wh));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < V; ++i) sv[i] = 0.0f;
+                    }
+                }
+            }
+        } else {
+            constexpr int CK = EPT < 8 ? EPT : 8;
+#pragma unroll
+            for (int k0 = 0; k0 < EPT; k0 += CK) {
+                float xv[CK], rv[CK];
+#pragma unroll
+                for (int k = 0; k < CK; ++k) {
+                    const int col = t + (k0 + k) * nt;
+                    if (col < p.H) {
+                        xv[k] = C::load1(xr + int64_t(col) * sizeof(T));
+                        rv[k] = C::load1(rr + int64_t(col) * sizeof(T));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < CK; ++k) {
+                    const int col = t + (k0 + k) * nt;
+                    s[k0 + k] = 0.0f;
+                    if (col < p.H) {
+                        s[k0 + k] = xv[k] + rv[k];
+                        acc2(ss, sc, s[k0 + k] * s[k0 + k]);
+                        C::store1(hr + int64_t(col) * sizeof(T), s[k0 + k]);
+                    }
+                }
+            }
+        }
+        const float total = block_sum(ss + sc, red);
+        const float rstd = 1.0f / sqrtf(total / float(p.H) + p.eps);
+        if (t == 0 && p.rstd) p.rstd[row] = rstd;
+        if constexpr (VEC) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int col = (t + k * nt) * V;
+                if (col < p.H) {
+                    uint32_t wg[W], wy[W];
+                    Access<16>::load(p.gamma + int64_t(col) * sizeof(T), reinterpret_cast<uint32_t(&)[4]>(wg));
+#pragma unroll
+                    for (int j = 0; j < W; ++j) {
+                        float f[C::kPerWord];
+#pragma unroll
+                        for (int e = 0; e < C::kPerWord; ++e)
+                            f[e] = s[k * V + j * C::kPerWord + e] * rstd * C::get(wg[j], e);
+                        wy[j] = C::put(f);
+                    }
+                    Access<16>::store(yr + int64_t(col) * sizeof(T), reinterpret_cast<const uint32_t(&)[4]>(wy));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const int col = t + k * nt;
+                if (col < p.H)
+                    C::store1(yr + int64_t(col) * sizeof(T), s[k] * rstd * C::load1(p.gamma + int64_t(col) * sizeof(T)));
+            }
+        }
+    }
+}
+
+using KernelFn = void (*)(Params);
+
+template <class T>
+KernelFn pick_t(int ept, bool vec)
+{
+    if (vec) return ept == 16 ? add_rmsnorm_kernel<T, 16, true> : add_rmsnorm_kernel<T, 64, true>;
+    return ept == 16 ? add_rmsnorm_kernel<T, 16, false> : add_rmsnorm_kernel<T, 64, false>;
+}
+
+KernelFn pick(int dtype, int ept, bool vec)
+{
+    switch (dtype) {
+    case GLU_F32: return pick_t<float>(ept, vec);
+    case GLU_F16: return pick_t<__half>(ept, vec);
+    default: return pick_t<__nv_bfloat16>(ept, vec);
+    }
+}
+
+}  // namespace rms
+}  // namespace glu
+
+extern "C" int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride, const void *residual, int64_t res_stride,
+                                   const void *gamma, void *h, int64_t h_stride, void *y, int64_t y_stride,
+                                   float *rstd, int64_t n_rows, int64_t n_cols, float eps, glu_dtype_t dtype,
+                                   glu_stream_t stream)
+{
+    using namespace glu::rms;
+    bool empty = false;
+    const int st = glu::validate_add_rmsnorm(x, x_stride, residual, res_stride, gamma, h, h_stride, y, y_stride,
+                                             rstd, n_rows, n_cols, eps, dtype, &empty);
+    if (st != GLU_OK) return st;
+    if (empty) {
+        glu::record_launch(glu_launch_info_t{});
+        return GLU_OK;
+    }
+    const int E = dtype == GLU_F32 ? 4 : 2;
+    if (n_rows == 1) x_stride = res_stride = h_stride = y_stride = n_cols;
+    const auto a16 = [](const void *q) { return uintptr_t(q) % 16 == 0; };
+    const bool vec = a16(x) && a16(residual) && a16(gamma) && a16(h) && a16(y) && (n_cols * E) % 16 == 0 &&
+                     (x_stride * E) % 16 == 0 && (res_stride * E) % 16 == 0 && (h_stride * E) % 16 == 0 &&
+                     (y_stride * E) % 16 == 0;
+    // 16 fp32 elements per thread up to 16384 columns (at most 1024 threads),
+    // else 64 (at most 512 threads)
+    const int ept = n_cols <= 16 * 1024 ? 16 : 64;
+    int threads = int((n_cols + ept - 1) / ept);
+    threads = (threads + 31) / 32 * 32;
+    Params p{};
+    p.x = static_cast<const char *>(x);
+    p.res = static_cast<const char *>(residual);
+    p.gamma = static_cast<const char *>(gamma);
+    p.h = static_cast<char *>(h);
+    p.y = static_cast<char *>(y);
+    p.rstd = rstd;
+    p.sx = x_stride * E;
+    p.sr = res_stride * E;
+    p.sh = h_stride * E;
+    p.sy = y_stride * E;
+    p.rows = n_rows;
+    p.H = int(n_cols);
+    p.eps = eps;
+    const unsigned grid = unsigned(n_rows < int64_t(INT32_MAX) ? n_rows : int64_t(INT32_MAX));
+    KernelFn fn = pick(dtype, ept, vec);
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(unsigned(threads));
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {&p};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return glu::cuda_fail(e);
+    }
+    glu_launch_info_t info{};
+    info.launched = 1;
+    info.vec_bytes = vec ? 16 : E;
+    info.unroll = ept;
+    info.threads = threads;
+    info.grid = int32_t(grid);
+    info.path = 4;
+    info.vector_units = n_rows;
+    glu::record_launch(info);
+    return GLU_OK;
+}

@@ -148,3 +148,18 @@ def gemm_llama(seed: int = 7, M: int = 4096, K: int = 4096, I: int = 14336, dtyp
     s = float(1.0 / np.sqrt(K))
     return {"x": normal_bits(rng, (M, K), 1.0, dtype), "w_gate": normal_bits(rng, (I, K), s, dtype),
             "w_up": normal_bits(rng, (I, K), s, dtype), "dtype": dtype}
+
+
+# ---------------------------------------------------------------------------
+# Residual add + RMSNorm.
+# ---------------------------------------------------------------------------
+
+def add_rmsnorm(seed: int = 8, rows: int = 4096, H: int = 4096, dtype: str = "bf16"):
+    """One decoder block's residual add + RMSNorm: x (the sub-block's output) ~
+    N(0, 1), the residual stream ~ N(0, 4^2) (it grows over the layers),
+    gamma ~ 1 + N(0, 0.1^2), eps = 1e-5."""
+    rng = np.random.default_rng([seed, rows, H, SWEEP_DTYPES.index(dtype)])
+    x = normal_bits(rng, (rows, H), 1.0, dtype)
+    res = normal_bits(rng, (rows, H), 4.0, dtype)
+    g = rng.standard_normal(size=H, dtype=np.float32) * np.float32(0.1) + np.float32(1.0)
+    return {"x": x, "res": res, "gamma": f32_to_bits(g, dtype), "eps": 1e-5, "dtype": dtype}

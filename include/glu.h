@@ -96,7 +96,8 @@ typedef enum {
     GLU_ERR_ALIAS = -4,   /* outputs overlap inputs other than exactly, or each other */
     GLU_ERR_ENUM = -5,    /* unknown act, layout or dtype */
     GLU_ERR_CUDA = -6,    /* the CUDA runtime refused a launch or copy; see glu_last_cuda_error() */
-    GLU_ERR_WORKSPACE = -7  /* host-memory entry points: workspace NULL or too small for one row */
+    GLU_ERR_WORKSPACE = -7, /* host-memory entry points: workspace NULL or too small for one row */
+    GLU_ERR_VALUE = -8      /* a numeric argument out of range (glu_add_rmsnorm_fwd: eps) */
 } glu_status_t;
 
 /*
@@ -333,6 +334,45 @@ int glu_gemm_fwd(const void *x, int64_t x_stride,
                  void *y, int64_t y_stride,
                  int64_t M, int64_t K, int64_t I,
                  glu_act_t act, glu_dtype_t dtype, glu_stream_t stream);
+
+/*
+ * Fused residual add + RMSNorm ("Skill: Write a Triton Fused Add+RMSNorm
+ * Kernel": Purpose; Required reasoning process steps 1-9; Kernel design rules;
+ * Correctness requirements), over each row r < n_rows of H = n_cols elements:
+ *
+ *     s[r, j] = x[r, j] + residual[r, j]             (fp32; exact for 16-bit inputs)
+ *     h[r, j] = round(s[r, j])                        (the residual stream for the next block)
+ *     rstd[r] = 1 / sqrt(sum_j s[r, j]^2 / H + eps)   (eps inside the root)
+ *     y[r, j] = round(s[r, j] * rstd[r] * gamma[j])   (gamma indexed by column only)
+ *
+ * No mean is subtracted and there is no bias.  Arithmetic is fp32 from the add
+ * through the product; each stored value is rounded to nearest-even once.
+ *
+ *   x, x_stride          input rows (row-major, element strides, >= n_cols).
+ *   residual, res_stride the residual rows.
+ *   gamma                n_cols elements of `dtype`, shared by every row.
+ *   h, h_stride          output: the summed rows.  May be exactly x or exactly
+ *                        residual (same pointer and stride): in place.
+ *   y, y_stride          output: the normalised rows.  May be exactly x or
+ *                        residual when h is not the same one; h and y must not
+ *                        overlap.  Other overlaps with an input: GLU_ERR_ALIAS.
+ *   rstd                 NULL, or n_rows floats receiving rstd (kept for a
+ *                        backward pass); must not overlap any matrix.
+ *   eps                  > 0 and finite, else GLU_ERR_VALUE.
+ *   n_cols               at most 32768 (a row lives in registers), else
+ *                        GLU_ERR_SHAPE.
+ * All pointers are device pointers; the call is asynchronous on `stream`.
+ * n_rows == 0 or n_cols == 0 returns GLU_OK without launching.
+ * Returns GLU_OK or a negative glu_status_t.
+ */
+int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride,
+                        const void *residual, int64_t res_stride,
+                        const void *gamma,
+                        void *h, int64_t h_stride,
+                        void *y, int64_t y_stride,
+                        float *rstd,
+                        int64_t n_rows, int64_t n_cols, float eps,
+                        glu_dtype_t dtype, glu_stream_t stream);
 
 #ifdef __cplusplus
 }

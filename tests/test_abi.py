@@ -2,8 +2,9 @@
 declares, and its host-side validation returns the documented status codes.
 
 No test here enqueues GPU work.  Fake device addresses are only ever passed to
-calls that must be rejected before any launch; the one test that lets a valid
-call reach the CUDA runtime is skipped whenever a GPU is present."""
+calls that must be rejected before any launch, and every test that passes them
+(including those that let a valid call reach the CUDA runtime, which fails for
+want of a device) is skipped whenever a GPU is present."""
 import os
 import re
 import subprocess
@@ -21,6 +22,10 @@ SPLIT, CONCAT = 0, 1
 SILU, RELU = 0, 3
 F32, F16, BF16 = 0, 1, 2
 BASE = 1 << 32          # fake, 4 KiB-aligned device addresses: never dereferenced
+
+# Tests that pass fake device addresses run only where no GPU is present: on a
+# GPU a validation mistake would launch a kernel on them.
+cpu_only = pytest.mark.skipif(torch.cuda.is_available(), reason="passes fake device addresses")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -68,6 +73,7 @@ def bwd(dc=BASE + (3 << 20), sdc=64, a=BASE, sa=64, b=BASE + (1 << 20), sb=64,
     return glu.glu_bwd(dc, sdc, a, sa, b, sb, da, sda, db, sdb, rows, cols, layout, act, dtype, None)
 
 
+@cpu_only
 def test_bad_enums():
     assert fwd(layout=2) == ENUM
     assert fwd(act=4) == ENUM and fwd(act=-1) == ENUM
@@ -75,6 +81,7 @@ def test_bad_enums():
     assert bwd(layout=7) == ENUM and bwd(act=9) == ENUM and bwd(dtype=-2) == ENUM
 
 
+@cpu_only
 def test_shapes():
     assert fwd(rows=-1) == SHAPE and fwd(cols=-5) == SHAPE
     assert bwd(rows=-1) == SHAPE
@@ -82,6 +89,7 @@ def test_shapes():
     assert fwd(rows=1 << 40, sa=1 << 30, sb=1 << 30, sy=1 << 30, cols=1 << 30) == SHAPE
 
 
+@cpu_only
 def test_empty_is_a_noop_even_with_null_pointers():
     assert fwd(a=None, b=None, y=None, rows=0) == OK
     assert fwd(a=None, b=None, y=None, cols=0) == OK
@@ -89,13 +97,16 @@ def test_empty_is_a_noop_even_with_null_pointers():
     assert glu.glu_last_launch()["launched"] == 0
 
 
+@cpu_only
 def test_null_pointers():
     assert fwd(a=None) == NULL and fwd(b=None) == NULL and fwd(y=None) == NULL
-    assert fwd(b=None, layout=CONCAT, sa=128) != NULL          # b is ignored for CONCAT
+    # b is ignored for CONCAT: the call gets past the NULL check and stops at y's stride
+    assert fwd(b=None, layout=CONCAT, sa=128, sy=3) == STRIDE
     for k in ("dc", "a", "b", "da", "db"):
         assert bwd(**{k: None}) == NULL, k
 
 
+@cpu_only
 def test_strides():
     assert fwd(sa=63) == STRIDE and fwd(sb=10) == STRIDE and fwd(sy=0) == STRIDE
     assert fwd(sa=-64) == STRIDE
@@ -104,6 +115,7 @@ def test_strides():
     assert bwd(layout=CONCAT, sa=128, sda=127) == STRIDE
 
 
+@cpu_only
 def test_partial_aliasing_is_rejected():
     # y shifted by one element against b
     assert fwd(y=BASE + (1 << 20) + 2) == ALIAS
@@ -118,7 +130,7 @@ def test_partial_aliasing_is_rejected():
     assert fwd(layout=CONCAT, sa=128, y=BASE + 2, sy=128) == ALIAS
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake addresses")
+@cpu_only
 def test_valid_calls_reach_the_cuda_runtime_without_a_gpu():
     """Exact aliasing and interleaved-but-disjoint rows pass validation; with no
     GPU the launch then fails cleanly with GLU_ERR_CUDA and a message."""
@@ -196,13 +208,14 @@ def test_fastdiv_host_logic(tmp_path):
     exe = tmp_path / "fd"
     csrc = os.path.join(ROOT, "glu_activation_mlps_gb300", "csrc")
     cuda_inc = "/usr/local/cuda/include"
-    subprocess.run(["g++", "-O2", "-std=c++17", f"-I{csrc}", f"-I{cuda_inc}", str(src), "-o", str(exe)],
-                   check=True)
+    subprocess.run(["g++", "-O2", "-std=c++17", f"-I{csrc}", f"-I{os.path.join(ROOT, 'include')}",
+                    f"-I{cuda_inc}", str(src), "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     checked, bad = map(int, out.stdout.split())
     assert out.returncode == 0 and bad == 0 and checked > 1_000_000
 
 
+@cpu_only
 def test_host_entry_points_validate_before_any_cuda_call():
     WS = BASE + (8 << 20)
     fh = lambda **k: glu.glu_fwd_host(*[k.get(n, d) for n, d in (
@@ -238,6 +251,7 @@ def gemm(x=BASE, sx=64, wg=BASE + (1 << 20), wu=BASE + (2 << 20), sw=64, y=BASE 
     return glu.glu_gemm_fwd(x, sx, wg, wu, sw, y, sy, M, K, I, act, dtype, None)
 
 
+@cpu_only
 def test_gemm_validation():
     assert gemm(dtype=F32) == ENUM and gemm(dtype=3) == ENUM and gemm(act=4) == ENUM
     assert gemm(M=-1) == SHAPE and gemm(K=-1) == SHAPE and gemm(I=1 << 31) == SHAPE
@@ -253,9 +267,47 @@ def test_gemm_validation():
     assert gemm(y=BASE + (1 << 20) - 4) == ALIAS
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake addresses")
+@cpu_only
 def test_gemm_valid_call_reaches_the_cuda_runtime_without_a_gpu():
     # y may be unaligned and strided; the inputs may overlap one another
     assert gemm(y=BASE + (3 << 20) + 2, sy=101) == CUDA
     assert gemm(wu=BASE + (1 << 20)) == CUDA
     assert glu.glu_last_cuda_error()
+
+
+# ---- glu_add_rmsnorm_fwd -----------------------------------------------------
+
+VALUE = -8
+
+
+def rms(x=BASE, sx=64, r=BASE + (1 << 20), sr=64, g=BASE + (2 << 20), h=BASE + (3 << 20), sh=64,
+        y=BASE + (4 << 20), sy=64, rstd=BASE + (5 << 20), rows=4, cols=64, eps=1e-5, dtype=BF16):
+    return glu.glu_add_rmsnorm_fwd(x, sx, r, sr, g, h, sh, y, sy, rstd, rows, cols, eps, dtype, None)
+
+
+@cpu_only
+def test_add_rmsnorm_validation():
+    assert rms(dtype=3) == ENUM and rms(dtype=-1) == ENUM
+    assert rms(rows=-1) == SHAPE and rms(cols=-2) == SHAPE
+    assert rms(cols=32769, sx=40000, sr=40000, sh=40000, sy=40000) == SHAPE
+    for bad in (0.0, -1e-5, float("nan"), float("inf")):
+        assert rms(eps=bad) == VALUE, bad
+    assert rms(x=None, r=None, g=None, h=None, y=None, rstd=None, rows=0) == OK
+    for k in ("x", "r", "g", "h", "y"):
+        assert rms(**{k: None}) == NULL, k
+    assert rms(sx=63) == STRIDE and rms(sh=10) == STRIDE and rms(sy=0) == STRIDE
+    # outputs: exactly an input is fine (checked with a GPU); any other overlap is not
+    assert rms(h=BASE + 2) == ALIAS                                 # h one element past x
+    assert rms(h=BASE + (3 << 20), y=BASE + (3 << 20) + 64) == ALIAS   # h and y overlap
+    assert rms(h=BASE, y=BASE) == ALIAS                             # both over x
+    assert rms(y=BASE + (2 << 20) + 6) == ALIAS                     # y over gamma
+    assert rms(rstd=BASE + 8) == ALIAS and rms(rstd=BASE + (4 << 20) + 100) == ALIAS
+    assert glu.glu_status_string(VALUE) != "unknown status"
+
+
+@cpu_only
+def test_add_rmsnorm_valid_calls_reach_the_cuda_runtime_without_a_gpu():
+    assert rms() == CUDA                                  # out of place
+    assert rms(h=BASE, y=BASE + (1 << 20)) == CUDA        # h over x, y over the residual
+    assert rms(h=BASE + (1 << 20), y=BASE, rstd=None) == CUDA
+    assert rms(x=BASE + 2, sx=67, cols=61) == CUDA        # unaligned: element accesses
