@@ -11,14 +11,16 @@
 // stays in L2 ("Performance requirements": the single-pass case).  Every
 // element is loaded and stored by one thread, its loads before its stores, and
 // y is stored only after the whole block has loaded its row, which makes h or
-// y written over x or the residual safe.  The sum of squares is compensated
-// within each thread, then reduced over the warp and the block in fp32; rstd
-// uses IEEE division and square root.
+// y written over x or the residual safe.  The sum of squares is formed with
+// fused multiply-adds in partial sums of 8 elements per thread, then reduced
+// over the warp and the block in fp32; rstd uses IEEE division and square root.
 //
 // Rows whose operands are 16-byte aligned (bases, strides and row width) use
 // 16-byte accesses, element i of a thread's k-th vector at column
-// (t + k * threads) * V + i; other rows use element accesses at column
-// t + k * threads.  Either way consecutive threads touch consecutive addresses.
+// (t + k * threads) * V + i, in a persistent grid (add_rmsnorm_rows_kernel);
+// other rows use element accesses at column t + k * threads, one block per row
+// (add_rmsnorm_kernel).  Either way consecutive threads touch consecutive
+// addresses.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -49,7 +51,10 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// Sum of v over the block; every thread gets the result.  `red` holds 33 floats.
+// Sum of v over the block; every thread gets the result.  `red` holds 33
+// floats; consecutive rows alternate between two such arrays, so the array a
+// row reads is not written again until every thread has passed the next row's
+// first barrier.
 __device__ __forceinline__ float block_sum(float v, float *red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -62,18 +67,35 @@ __device__ __forceinline__ float block_sum(float v, float *red)
         if (lane == 0) red[32] = w;
     }
     __syncthreads();
-    const float r = red[32];
-    __syncthreads();            // red is reused by the next row
-    return r;
+    return red[32];
 }
 
-// Compensated accumulation (Neumaier): s + c carries the running sum.
-__device__ __forceinline__ void acc2(float &s, float &c, float t)
-{
-    const float u = s + t;
-    c += fabsf(s) >= fabsf(t) ? (s - u) + t : (t - u) + s;
-    s = u;
-}
+// Sum of squares of a thread's elements: fused multiply-adds into partial sums
+// of (at most) 8 elements each, added pairwise at the end.  With the 5 + 5
+// additions of the warp and block reduction, every sum a block forms carries at
+// most 8 + 3 + 10 = 21 fp32 roundings of non-negative terms.
+template <int N>
+struct SumSq {
+    static constexpr int P = N / 8 > 0 ? N / 8 : 1;
+    float part[P];
+    __device__ __forceinline__ SumSq()
+    {
+#pragma unroll
+        for (int i = 0; i < P; ++i) part[i] = 0.0f;
+    }
+    __device__ __forceinline__ void add(int i, float f) { part[(i / 8) % P] = fmaf(f, f, part[(i / 8) % P]); }
+    __device__ __forceinline__ float total() const
+    {
+        float q[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) q[i] = part[i];
+#pragma unroll
+        for (int w = 1; w < P; w *= 2)
+#pragma unroll
+            for (int i = 0; i + w < P; i += 2 * w) q[i] += q[i + w];
+        return q[0];
+    }
+};
 
 template <class T, int EPT, bool VEC>
 __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
@@ -83,17 +105,18 @@ __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
     constexpr int V = VEC ? 16 / int(sizeof(T)) : 1;      // elements per access
     constexpr int NV = EPT / V;                           // accesses per thread per operand
     constexpr int W = V / C::kPerWord > 0 ? V / C::kPerWord : 1;   // 32-bit words per access
-    __shared__ float red[33];
+    __shared__ float red[2][33];
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int t = threadIdx.x, nt = blockDim.x;
-    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, parity ^= 1) {
         const char *xr = p.x + row * p.sx, *rr = p.res + row * p.sr;
         char *hr = p.h + row * p.sh, *yr = p.y + row * p.sy;
         float s[EPT];
-        float ss = 0.0f, sc = 0.0f;
+        SumSq<EPT> ss;
         // loads go out in chunks of CK accesses per operand, all of a chunk's
         // loads before its stores (each element is loaded and stored by this
         // thread alone, so h over x or the residual stays correct)
@@ -123,7 +146,7 @@ __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
                             for (int e = 0; e < C::kPerWord; ++e) {
                                 f[e] = C::get(wx[k][j], e) + C::get(wr[k][j], e);
                                 sv[j * C::kPerWord + e] = f[e];
-                                acc2(ss, sc, f[e] * f[e]);
+                                ss.add((k0 + k) * V + j * C::kPerWord + e, f[e]);
                             }
                             wh[j] = C::put(f);
                         }
@@ -153,13 +176,13 @@ __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
                     s[k0 + k] = 0.0f;
                     if (col < p.H) {
                         s[k0 + k] = xv[k] + rv[k];
-                        acc2(ss, sc, s[k0 + k] * s[k0 + k]);
+                        ss.add(k0 + k, s[k0 + k]);
                         C::store1(hr + int64_t(col) * sizeof(T), s[k0 + k]);
                     }
                 }
             }
         }
-        const float total = block_sum(ss + sc, red);
+        const float total = block_sum(ss.total(), red[parity]);
         const float rstd = 1.0f / sqrtf(total / float(p.H) + p.eps);
         if (t == 0 && p.rstd) p.rstd[row] = rstd;
         if constexpr (VEC) {
@@ -191,21 +214,116 @@ __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
     }
 }
 
+// The 16-byte path as a persistent grid: every thread owns the same columns in
+// every row, so gamma is read into registers once; the next row's x and
+// residual are requested before this row's reduction starts, so a block always
+// has loads in flight; s = x + residual is recomputed from the raw words for y
+// (exact for 16-bit inputs, the same fp32 rounding for f32) instead of being
+// held in registers.
+template <class T, int EPT>
+__global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
+    add_rmsnorm_rows_kernel(const Params p)
+{
+    using C = Codec<T>;
+    constexpr int V = 16 / int(sizeof(T));
+    constexpr int NV = EPT / V;
+    constexpr int W = 4;
+    __shared__ float red[2][33];
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const int t = threadIdx.x, nt = blockDim.x;
+    bool on[NV];
+    uint32_t gw[NV][W];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int col = (t + k * nt) * V;
+        on[k] = col < p.H;
+        if (on[k]) Access<16>::load(p.gamma + int64_t(col) * sizeof(T), gw[k]);
+    }
+    const auto load_row = [&](int64_t row, uint32_t (&wx)[NV][W], uint32_t (&wr)[NV][W]) {
+        const char *xr = p.x + row * p.sx, *rr = p.res + row * p.sr;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (on[k]) {
+                const int64_t off = int64_t((t + k * nt) * V) * sizeof(T);
+                Access<16>::load(xr + off, wx[k]);
+                Access<16>::load(rr + off, wr[k]);
+            }
+    };
+
+    uint32_t ax[NV][W], ar[NV][W];
+    int64_t row = blockIdx.x;
+    int parity = 0;
+    if (row < p.rows) load_row(row, ax, ar);
+    while (row < p.rows) {
+        const int64_t next = row + gridDim.x;
+        uint32_t bx[NV][W], br[NV][W];
+        if (next < p.rows) load_row(next, bx, br);
+        char *hr = p.h + row * p.sh, *yr = p.y + row * p.sy;
+        SumSq<EPT> ss;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (on[k]) {
+                uint32_t wh[W];
+#pragma unroll
+                for (int j = 0; j < W; ++j) {
+                    float f[C::kPerWord];
+#pragma unroll
+                    for (int e = 0; e < C::kPerWord; ++e) {
+                        f[e] = C::get(ax[k][j], e) + C::get(ar[k][j], e);
+                        ss.add(k * V + j * C::kPerWord + e, f[e]);
+                    }
+                    wh[j] = C::put(f);
+                }
+                Access<16>::store(hr + int64_t((t + k * nt) * V) * sizeof(T), wh);
+            }
+        const float total = block_sum(ss.total(), red[parity]);
+        parity ^= 1;
+        const float rstd = 1.0f / sqrtf(total / float(p.H) + p.eps);
+        if (t == 0 && p.rstd) p.rstd[row] = rstd;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            if (on[k]) {
+                uint32_t wy[W];
+#pragma unroll
+                for (int j = 0; j < W; ++j) {
+                    float f[C::kPerWord];
+#pragma unroll
+                    for (int e = 0; e < C::kPerWord; ++e)
+                        f[e] = (C::get(ax[k][j], e) + C::get(ar[k][j], e)) * rstd * C::get(gw[k][j], e);
+                    wy[j] = C::put(f);
+                }
+                Access<16>::store(yr + int64_t((t + k * nt) * V) * sizeof(T), wy);
+            }
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                ax[k][j] = bx[k][j];
+                ar[k][j] = br[k][j];
+            }
+        row = next;
+    }
+}
+
 using KernelFn = void (*)(Params);
 
 template <class T>
-KernelFn pick_t(int ept, bool vec)
+KernelFn pick_t(int ept, bool vec, bool rows)
 {
+    if (rows) return add_rmsnorm_rows_kernel<T, 16 / sizeof(T) * 2>;       // 16 (16-bit) or 8 (f32)
     if (vec) return ept == 16 ? add_rmsnorm_kernel<T, 16, true> : add_rmsnorm_kernel<T, 64, true>;
     return ept == 16 ? add_rmsnorm_kernel<T, 16, false> : add_rmsnorm_kernel<T, 64, false>;
 }
 
-KernelFn pick(int dtype, int ept, bool vec)
+KernelFn pick(int dtype, int ept, bool vec, bool rows)
 {
     switch (dtype) {
-    case GLU_F32: return pick_t<float>(ept, vec);
-    case GLU_F16: return pick_t<__half>(ept, vec);
-    default: return pick_t<__nv_bfloat16>(ept, vec);
+    case GLU_F32: return pick_t<float>(ept, vec, rows);
+    case GLU_F16: return pick_t<__half>(ept, vec, rows);
+    default: return pick_t<__nv_bfloat16>(ept, vec, rows);
     }
 }
 
@@ -232,9 +350,14 @@ extern "C" int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride, const void *
     const bool vec = a16(x) && a16(residual) && a16(gamma) && a16(h) && a16(y) && (n_cols * E) % 16 == 0 &&
                      (x_stride * E) % 16 == 0 && (res_stride * E) % 16 == 0 && (h_stride * E) % 16 == 0 &&
                      (y_stride * E) % 16 == 0;
-    // 16 fp32 elements per thread up to 16384 columns (at most 1024 threads),
-    // else 64 (at most 512 threads)
-    const int ept = n_cols <= 16 * 1024 ? 16 : 64;
+    // 16-byte rows of 16 KiB or more that fit 1024 threads of two 16-byte
+    // accesses per operand (16 elements of 16-bit types, 8 of f32) take the
+    // persistent kernel (measured on GB300: 4 % faster at 32 KiB rows, equal at
+    // 16 KiB, 1-5 % slower below); otherwise one block per row with 16
+    // elements per thread up to 16384 columns (at most 1024 threads), 64
+    // beyond (at most 512 threads)
+    const bool rows_kernel = vec && n_cols * E >= 16384 && n_cols <= int64_t(1024) * (32 / E);
+    const int ept = rows_kernel ? 32 / E : (n_cols <= 16 * 1024 ? 16 : 64);
     int threads = int((n_cols + ept - 1) / ept);
     threads = (threads + 31) / 32 * 32;
     Params p{};
@@ -251,8 +374,22 @@ extern "C" int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride, const void *
     p.rows = n_rows;
     p.H = int(n_cols);
     p.eps = eps;
-    const unsigned grid = unsigned(n_rows < int64_t(INT32_MAX) ? n_rows : int64_t(INT32_MAX));
-    KernelFn fn = pick(dtype, ept, vec);
+    KernelFn fn = pick(dtype, ept, vec, rows_kernel);
+    int64_t blocks = n_rows;
+    if (rows_kernel) {      // persistent: as many blocks as fit on the GPU at once
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void *>(fn), threads, 0);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return glu::cuda_fail(e);
+        }
+        const int64_t slots = int64_t(sms) * (per_sm > 0 ? per_sm : 1);
+        blocks = n_rows < slots ? n_rows : slots;
+    }
+    const unsigned grid = unsigned(blocks < int64_t(INT32_MAX) ? blocks : int64_t(INT32_MAX));
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
