@@ -68,13 +68,14 @@ struct Shape {
     static constexpr int kMmaM = BM * CTAS;
     static constexpr int kMmaN = 2 * BN;
     static constexpr int kAccCols = 2 * BN;                           // [gate | up] of one tile
-    static constexpr int kTmemCols = 2 * kAccCols;                    // two tiles in flight
+    // two tiles in flight, in a power-of-two allocation
+    static constexpr int kTmemCols = 2 * kAccCols <= 256 ? 256 : 512;
     static constexpr int kBars = 2 * kStages + 2 + 2 + 1;             // full, empty, acc_full, acc_empty, done
     static constexpr int kStageY = kEpiWarps * 2 * kYBox * kYBox * 2;  // two y boxes per epilogue warp
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStageY + kBars * 8 + 16;
     static_assert(CTAS == 1 || CTAS == 2, "one block or a pair");
     static_assert(BN % 32 == 0 && BN >= 32 && kMmaN <= 256, "one MMA covers N = 2 BN <= 256");
-    static_assert(kTmemCols == 256 || kTmemCols == 512, "a power-of-two column count");
+    static_assert(2 * kAccCols <= kTmemCols, "two accumulators fit the allocation");
     static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 };
@@ -87,6 +88,7 @@ struct Params {
     int m_blocks, i_blocks; // row blocks of 128 * CTAS rows, column blocks of BN
     int group_m;            // row blocks per group of the tile order
     int vec_store;          // y rows and base 16-byte aligned
+    uint32_t a_bytes;       // bytes of x one block's copy brings per stage (rows that exist, up to 128)
     int tma_store;          // the same: y leaves through shared memory and the tensor-memory accelerator
 };
 
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t st = saddr(smem + s * S::kStageBytes);
                     if constexpr (CTAS == 1) {
                         const uint32_t bar = saddr(&full[s]);
-                        arrive_expect_tx_local(bar, uint32_t(S::kStageBytes));
+                        arrive_expect_tx_local(bar, p.a_bytes + uint32_t(2 * S::kTileB));
                         tma_load<1>(st, &tm_x, kt * BK, m0, bar);
                         tma_load<1>(st + S::kTileA, &tm_wg, kt * BK, i0, bar);
                         tma_load<1>(st + S::kTileA + S::kTileB, &tm_wu, kt * BK, i0, bar);
@@ -624,7 +626,7 @@ KernelFn pick_act(int act)
 struct Variant {
     KernelFn fn;
     int smem;
-    int id;         // 0..3, see pick()
+    int id;         // 0..5, see pick()
 };
 
 template <int BN, int CTAS>
@@ -634,18 +636,41 @@ Variant variant(bool bf16, int act, int id)
             Shape<BN, CTAS>::kSmemBytes, id};
 }
 
-// One block per 128-row tile while M fits one row block, pairs of blocks on
-// 256 rows beyond that; 64-wide column tiles when I fits one.
 Variant pick(bool bf16, int act, int bn, int ctas)
 {
-    if (ctas == 1) return bn == 64 ? variant<64, 1>(bf16, act, 0) : variant<128, 1>(bf16, act, 1);
-    return bn == 64 ? variant<64, 2>(bf16, act, 2) : variant<128, 2>(bf16, act, 3);
+    if (ctas == 1) {
+        if (bn == 64) return variant<64, 1>(bf16, act, 0);
+        return bn == 96 ? variant<96, 1>(bf16, act, 1) : variant<128, 1>(bf16, act, 2);
+    }
+    if (bn == 64) return variant<64, 2>(bf16, act, 3);
+    return bn == 96 ? variant<96, 2>(bf16, act, 4) : variant<128, 2>(bf16, act, 5);
+}
+
+// Column-tile width: every tile of one width costs about the same, so the
+// launch takes ceil(tiles / slots) rounds of tiles BN columns wide; pick the
+// width with the fewest columns in its rounds (the widest on a tie: wider
+// tiles move fewer bytes per FLOP).  With 152 SMs and I = 14336, M <= 128
+// gets 96 (150 tiles, one round) instead of 128 (112 tiles on 152 SMs).
+int pick_bn(int64_t m_blocks, int64_t I, int64_t slots)
+{
+    if (I <= 64) return 64;
+    int best = 128;
+    int64_t best_cost = -1;
+    for (int bn : {128, 96, 64}) {
+        const int64_t tiles = m_blocks * ((I + bn - 1) / bn);
+        const int64_t cost = (tiles + slots - 1) / slots * bn;
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 // Per kernel variant and device: the shared-memory opt-in done, and how many
 // blocks (one shape) or pairs (the other) fit on the GPU at once.
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_slots[kMaxDevices][2][4][4];
+std::atomic<int> g_slots[kMaxDevices][2][4][6];
 
 bool overlap(uintptr_t a0, uint64_t alen, uintptr_t b0, uint64_t blen)
 {
@@ -700,13 +725,14 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
         return GLU_ERR_ALIAS;
 
     const bool bf16 = dtype == GLU_BF16;
-    const int bn = I <= 64 ? 64 : 128;
     const int ctas = M > BM ? 2 : 1;
-    const Variant v = pick(bf16, act, bn, ctas);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
+    const int64_t rows_per_block = int64_t(BM) * ctas;
+    const int bn = pick_bn((M + rows_per_block - 1) / rows_per_block, I, sms / ctas);
+    const Variant v = pick(bf16, act, bn, ctas);
 
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[2];
@@ -745,7 +771,11 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
 
     const bool y_aligned = (uintptr_t(y) % 16 == 0) && ((y_stride * E) % 16 == 0);
     CUtensorMap tx, tg, tu, ty;
-    if (!make_map(&tx, bf16, x, M, K, x_stride * E, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    // one block holding every row copies only the rows that exist (rounded up to
+    // a swizzle atom of 8): the MMA rows past them read stale shared memory and
+    // produce accumulator rows that are never stored
+    const int a_rows = ctas == 1 ? int((M + 7) / 8 * 8) : BM;
+    if (!make_map(&tx, bf16, x, M, K, x_stride * E, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tg, bf16, w_gate, I, K, w_stride * E, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tu, bf16, w_up, I, K, w_stride * E, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B))
         return glu::cuda_fail(cudaErrorInvalidValue);
@@ -763,7 +793,6 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     p.I = int(I);
     p.K = int(K);
     p.k_tiles = int((K + BK - 1) / BK);
-    const int64_t rows_per_block = int64_t(BM) * ctas;
     p.m_blocks = int((M + rows_per_block - 1) / rows_per_block);
     p.i_blocks = int((I + bn - 1) / bn);
     // row blocks per group: their x rows (about 48 MiB at most) stay in L2
@@ -773,6 +802,7 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     group = group < 1 ? 1 : (group > p.m_blocks ? p.m_blocks : group);
     p.group_m = int(group);
     p.vec_store = y_aligned;
+    p.a_bytes = uint32_t(a_rows) * BK * E;
     p.tma_store = y_map;
     const int64_t tiles = int64_t(p.m_blocks) * p.i_blocks;
     if (tiles * ctas > INT32_MAX) return GLU_ERR_SHAPE;

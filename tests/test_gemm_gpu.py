@@ -89,13 +89,33 @@ def check_bound(orc, act, dt, y_bits, g, u, sg, su, K, what):
 # ---------------------------------------------------------------- exact grid inputs, every output
 
 # M <= 128 runs one block per tile, larger M pairs of blocks on 256 rows;
-# I <= 64 takes 64-wide column tiles, larger I 128-wide ones.
+# column tiles are 64, 96 or 128 wide (the rule in expected_tiles), and the
+# shapes below take each width in both block shapes.
 SHAPES = [(1, 8, 1), (128, 64, 128), (127, 72, 65), (300, 200, 300), (129, 1000, 40), (257, 328, 200),
-          (64, 4096, 64), (700, 256, 520), (333, 136, 100)]
+          (64, 4096, 64), (700, 256, 520), (333, 136, 100), (5, 520, 14336), (256, 64, 14336),
+          (100, 64, 38912)]
 
 
 def cluster_size(M, I):
     return 1 if M <= 128 else 2
+
+
+def expected_tiles(M, I, sms):
+    """The library's tile-width rule: the width in {128, 96, 64} whose rounds of
+    tiles (ceil(tiles / slots) of them) span the fewest columns, the widest on a
+    tie; 64 when I fits one tile."""
+    ctas = cluster_size(M, I)
+    m_blocks = -(-M // (128 * ctas))
+    slots = sms // ctas
+    if I <= 64:
+        return m_blocks
+    best = None
+    for bn in (128, 96, 64):
+        tiles = m_blocks * -(-I // bn)
+        cost = -(-tiles // slots) * bn
+        if best is None or cost < best[0]:
+            best = (cost, tiles)
+    return best[1]
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -110,6 +130,8 @@ def test_grid_inputs_every_output(orc, shape, act, dt):
     y, _, _ = run_gemm(x, wg, wu, dt, act, K)
     info = glu.glu_last_launch()
     assert info["path"] == 3 and info["unroll"] == cluster_size(M, I) and info["grid"] % info["unroll"] == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert info["vector_units"] == expected_tiles(M, I, sms)
     ref = orc.gemm_glu(act, dt, x, wg, wu)
     compare(y, ref, dt, what=f"gemm {act} {dt} {shape}")
 
