@@ -68,6 +68,8 @@ def lib():
             L.oracle_gemm_glu_at.restype = None
             L.oracle_add_rmsnorm.argtypes = [ci, vp, vp, vp, vp, vp, dp, dp, i64, i64, ctypes.c_double]
             L.oracle_add_rmsnorm.restype = None
+            L.oracle_add_rmsnorm_bwd.argtypes = [ci, vp, vp, vp, vp, vp, vp, dp, dp, i64, i64]
+            L.oracle_add_rmsnorm_bwd.restype = None
             L.oracle_sigmoid.argtypes = [ctypes.c_double]
             L.oracle_sigmoid.restype = ctypes.c_double
             for f in (L.oracle_fwd, L.oracle_bwd, L.oracle_bwd_da_scale, L.oracle_act_vec,
@@ -279,3 +281,26 @@ def add_rmsnorm(dtype: str, x, res, gamma, eps: float):
     lib().oracle_add_rmsnorm(DTYPES[dtype], _ptr(x), _ptr(res), _ptr(gamma), _ptr(h), _ptr(y), _ptr(rstd),
                              _ptr(y_exact), rows, H, float(eps))
     return h, y, rstd, y_exact
+
+
+def add_rmsnorm_bwd(dtype: str, dy, h, rstd, gamma, dh=None):
+    """ds = rstd*gamma*dy - (rstd^3/H) * h * sum(gamma*dy*h) (+ dh), rounded once,
+    and dgamma = sum over rows of dy*h*rstd.  dy, h (and dh) are (rows, H) bit
+    arrays, rstd a float32 array of one value per row, gamma (H,) bits.
+    Returns (ds bits, ds exact, dgamma)."""
+    dy, h, gamma = _bits(dy, dtype), _bits(h, dtype), _bits(gamma, dtype)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float32)
+    if dy.ndim != 2 or h.shape != dy.shape or rstd.shape != (dy.shape[0],) or gamma.shape != (dy.shape[1],):
+        raise ValueError("dy, h are (rows, H), rstd (rows,), gamma (H,)")
+    rows, H = dy.shape
+    if dh is not None:
+        dh = _bits(dh, dtype)
+        if dh.shape != dy.shape:
+            raise ValueError("dh must match dy")
+    ds = np.empty_like(dy)
+    ds_exact = np.empty((rows, H))
+    dgamma = np.empty(H)
+    lib().oracle_add_rmsnorm_bwd(DTYPES[dtype], _ptr(dy), _ptr(h), _ptr(rstd), _ptr(gamma),
+                                 _ptr(dh) if dh is not None else None, _ptr(ds), _ptr(ds_exact), _ptr(dgamma),
+                                 rows, H)
+    return ds, ds_exact, dgamma

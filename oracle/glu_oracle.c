@@ -400,3 +400,41 @@ void oracle_add_rmsnorm(int dtype, const void *x, const void *res, const void *g
     }
     free(hv);
 }
+
+/* Backward of the residual add + RMSNorm ("Skill: Write a Triton Fused
+ * Add+RMSNorm Kernel", Required reasoning process steps 9-10: the forward keeps
+ * rstd and the summed rows; the gradient of the norm goes to x and to the
+ * residual alike).  With y = s * rstd * gamma and rstd = (sum s^2 / H + eps)^(-1/2),
+ *   ds[j]  = rstd * gamma[j] * dy[j] - (rstd^3 / H) * s[j] * sum_k gamma[k] dy[k] s[k]
+ *            (+ dh[j], the gradient reaching s through the residual stream)
+ *   dgamma[j] = sum over rows of dy[j] * s[j] * rstd
+ * s is the stored sum h, rstd the stored fp32 value (f32 bit patterns), both
+ * taken as given.  dh may be NULL.  Outputs: ds rounded once into the dtype,
+ * ds unrounded (may be NULL) and dgamma (H doubles, overwritten).  Contiguous
+ * rows. */
+void oracle_add_rmsnorm_bwd(int dtype, const void *dy, const void *h, const void *rstd_bits, const void *gamma,
+                            const void *dh, void *ds, double *ds_exact, double *dgamma, int64_t n_rows, int64_t H)
+{
+    for (int64_t j = 0; j < H; ++j) dgamma[j] = 0.0;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const double rs = oracle_decode(load_bits(rstd_bits, r, ORC_F32), ORC_F32);
+        double dot = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            const int64_t i = r * H + j;
+            dot += oracle_decode(load_bits(gamma, j, dtype), dtype) * oracle_decode(load_bits(dy, i, dtype), dtype) *
+                   oracle_decode(load_bits(h, i, dtype), dtype);
+        }
+        const double c = rs * rs * rs / (double)H * dot;
+        for (int64_t j = 0; j < H; ++j) {
+            const int64_t i = r * H + j;
+            const double g = oracle_decode(load_bits(gamma, j, dtype), dtype);
+            const double d = oracle_decode(load_bits(dy, i, dtype), dtype);
+            const double s = oracle_decode(load_bits(h, i, dtype), dtype);
+            double v = rs * g * d - c * s;
+            if (dh) v += oracle_decode(load_bits(dh, i, dtype), dtype);
+            store_bits(ds, i, dtype, oracle_encode(v, dtype));
+            if (ds_exact) ds_exact[i] = v;
+            dgamma[j] += d * s * rs;
+        }
+    }
+}

@@ -537,3 +537,80 @@ def test_add_rmsnorm_scale_invariance(orc):
     rs = _bf16(orc.decode("bf16", r) * 2.0 ** 40)
     _, _, _, ye2 = orc.add_rmsnorm("bf16", xs, rs, g, 1e-3 * 2.0 ** 80)
     assert np.allclose(ye, ye2, rtol=1e-14, atol=0)
+
+
+def _rmsnorm_setup(rng, rows, H, dt, eps):
+    h = glu_synth.normal_bits(rng, (rows, H), 3.0, dt)
+    dy = glu_synth.normal_bits(rng, (rows, H), 1.0, dt)
+    g = glu_synth.f32_to_bits(rng.standard_normal(H, dtype=np.float32) * np.float32(0.2) + np.float32(1.0), dt)
+    return h, dy, g
+
+
+def _exact_rstd(orc, dt, h, g, eps):
+    zero = np.zeros_like(h)
+    _, _, rstd, _ = orc.add_rmsnorm(dt, h, zero, g, eps)
+    return rstd
+
+
+def test_add_rmsnorm_bwd_matches_torch_autograd(orc):
+    """ds and dgamma against torch's float64 autograd through F.rms_norm, with
+    the rstd the forward keeps (fp32) in place of torch's own."""
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    rng = np.random.default_rng(60)
+    rows, H, eps = 4, 1024, 1e-5
+    h, dy, g = _rmsnorm_setup(rng, rows, H, "bf16", eps)
+    rstd = _exact_rstd(orc, "bf16", h, g, eps)
+    _, ds, dgamma = orc.add_rmsnorm_bwd("bf16", dy, h, rstd.astype(np.float32), g)
+    ht = torch.tensor(orc.decode("bf16", h), requires_grad=True)
+    gt = torch.tensor(orc.decode("bf16", g), requires_grad=True)
+    y = F.rms_norm(ht, (H,), weight=gt, eps=eps)
+    y.backward(torch.tensor(orc.decode("bf16", dy)))
+    scale = np.abs(ht.grad.numpy()).max()
+    assert np.allclose(ds, ht.grad.numpy(), rtol=1e-6, atol=1e-6 * scale)
+    assert np.allclose(dgamma, gt.grad.numpy(), rtol=1e-6, atol=1e-6 * np.abs(gt.grad.numpy()).max())
+
+
+def test_add_rmsnorm_bwd_finite_differences(orc):
+    """ds is the derivative of L = sum(dy * y) along h (central differences of
+    the forward oracle in f32 with steps of 2^-12 |h|)."""
+    rng = np.random.default_rng(61)
+    H, eps = 48, 0.3
+    h, dy, g = _rmsnorm_setup(rng, 1, H, "f32", eps)
+    rstd = _exact_rstd(orc, "f32", h, g, eps)
+    _, ds, _ = orc.add_rmsnorm_bwd("f32", dy, h, rstd.astype(np.float32), g)
+    hv = orc.decode("f32", h)[0]
+    dyv = orc.decode("f32", dy)[0]
+    zero = np.zeros((1, H), dtype=np.uint32)
+    for j in (0, 7, 31, 47):
+        step = 2.0 ** (np.floor(np.log2(abs(hv[j]))) - 12)
+        vals = []
+        for sgn in (1, -1):
+            hp = hv.copy()
+            hp[j] += sgn * step
+            _, _, _, ye = orc.add_rmsnorm("f32", glu_synth.f32_to_bits(hp[None, :].astype(np.float32), "f32"), zero,
+                                          g, eps)
+            vals.append(float(np.dot(dyv, ye[0])))
+        fd = (vals[0] - vals[1]) / (2 * step)
+        assert fd == pytest.approx(ds[0, j], rel=2e-5, abs=1e-6)
+
+
+def test_add_rmsnorm_bwd_identities(orc):
+    """sum_j ds_j s_j = rstd D (1 - rstd^2 mean(s^2)) with D = sum gamma dy s (the
+    gradient along s only rescales the norm term); dh is added unchanged; dgamma
+    sums its rows."""
+    rng = np.random.default_rng(62)
+    rows, H, eps = 3, 200, 1e-2
+    h, dy, g = _rmsnorm_setup(rng, rows, H, "f16", eps)
+    rstd = _exact_rstd(orc, "f16", h, g, eps).astype(np.float32)
+    _, ds, dgamma = orc.add_rmsnorm_bwd("f16", dy, h, rstd, g)
+    s, d, gv, rs = orc.decode("f16", h), orc.decode("f16", dy), orc.decode("f16", g), rstd.astype(np.float64)
+    D = np.sum(gv[None, :] * d * s, axis=1)
+    ms = np.mean(s * s, axis=1)
+    assert np.allclose(np.sum(ds * s, axis=1), rs * D * (1 - rs * rs * ms), rtol=1e-9, atol=1e-12)
+    dh = glu_synth.normal_bits(rng, (rows, H), 1.0, "f16")
+    _, ds2, dgamma2 = orc.add_rmsnorm_bwd("f16", dy, h, rstd, g, dh)
+    assert np.allclose(ds2 - ds, orc.decode("f16", dh), rtol=0, atol=1e-12)
+    assert np.array_equal(dgamma, dgamma2)
+    parts = [orc.add_rmsnorm_bwd("f16", dy[r:r + 1], h[r:r + 1], rstd[r:r + 1], g)[2] for r in range(rows)]
+    assert np.allclose(dgamma, np.sum(parts, axis=0), rtol=1e-14, atol=0)
