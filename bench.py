@@ -605,11 +605,47 @@ def run_rmsnorm(args):
                 "speedup_vs_unfused": round(ms_unfused / ms, 3), "bytes": nbytes, "launch": info,
                 "buffer_sets": nsets}
 
+    def backward(rows, H):
+        """glu_add_rmsnorm_bwd (dx, dgamma) against torch autograd through add +
+        F.rms_norm; algorithmic bytes: read dy and h, write dx (3 row passes)."""
+        E = 2
+        nsets = max(2, -(-3 * L2_BYTES // (3 * rows * H * E)))
+        sets = [((torch.randn(rows, H, device=dev, generator=gen)).to(torch.bfloat16),
+                 (torch.randn(rows, H, device=dev, generator=gen) * 4).to(torch.bfloat16),
+                 torch.empty(rows, H, device=dev, dtype=torch.bfloat16)) for _ in range(nsets)]
+        g = (1 + 0.1 * torch.randn(H, device=dev, generator=gen)).to(torch.bfloat16)
+        rstd = (0.2 + 0.5 * torch.rand(rows, device=dev, generator=gen)).float()
+        dgam = torch.zeros(H, device=dev, dtype=torch.float32)
+
+        def fused(k):
+            dy, h, dx = sets[k]
+            st = L.glu_add_rmsnorm_bwd(dy.data_ptr(), H, h.data_ptr(), H, rstd.data_ptr(), g.data_ptr(), None, 0,
+                                       dx.data_ptr(), H, None, 0, dgam.data_ptr(), rows, H, 2, s)
+            if st:
+                raise glu.GluError(st, "glu_add_rmsnorm_bwd")
+
+        ms = timed(fused, nsets)
+        info = glu.glu_last_launch()
+        # torch: the same gradients through autograd of add + rms_norm
+        xs = [sets[k][1].clone().requires_grad_(True) for k in range(nsets)]
+        gt = g.clone().requires_grad_(True)
+        graphs = [F.rms_norm(xs[k] + 0, (H,), gt, 1e-5) for k in range(nsets)]
+
+        def unfused(k):
+            torch.autograd.grad(graphs[k], (xs[k], gt), sets[k][0], retain_graph=True)
+
+        ms_t = timed(unfused, nsets)
+        nbytes = 3 * rows * H * E + H * E + 4 * rows + 4 * H
+        return {"rows": rows, "H": H, "ms": round(ms, 5), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "torch_autograd_ms": round(ms_t, 5),
+                "speedup_vs_torch": round(ms_t / ms, 3), "bytes": nbytes, "launch": info}
+
     clocks = ClockSampler(gpu_selector(0))
     clocks.start()
     main = case(4096, 4096, clocks)
     clock_info = clocks.stop()
     sweep = [case(4096, H) for H in (1024, 2048, 8192, 16384)]
+    bwd = [backward(4096, H) for H in (1024, 4096, 16384)]
     line = {
         "metric": "fused residual add + RMSNorm achieved HBM GB/s (bf16, 4096 tokens x hidden 4096)",
         "value": main["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
@@ -625,6 +661,7 @@ def run_rmsnorm(args):
                        "speedup_vs_unfused": main["speedup_vs_unfused"]},
         "sweep": [{k: c[k] for k in ("rows", "H", "ms", "gbs", "frac", "torch_unfused_ms", "speedup_vs_unfused")}
                   for c in sweep],
+        "backward": bwd,
         "gpu_launches": K,
         "clocks": clock_info,
     }

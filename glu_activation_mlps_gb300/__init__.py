@@ -33,7 +33,7 @@ EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_fwd_host_n
            "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
            "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_gemm_fwd",
-           "glu_add_rmsnorm_fwd")
+           "glu_add_rmsnorm_fwd", "glu_add_rmsnorm_bwd")
 
 
 class GluError(RuntimeError):
@@ -112,6 +112,9 @@ def lib() -> ctypes.CDLL:
             L.glu_add_rmsnorm_fwd.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i64, vp, i64, i64,
                                               ctypes.c_float, ci, vp]
             L.glu_add_rmsnorm_fwd.restype = ci
+            L.glu_add_rmsnorm_bwd.argtypes = [vp, i64, vp, i64, vp, vp, vp, i64, vp, i64, vp, i64, vp, i64, i64,
+                                              ci, vp]
+            L.glu_add_rmsnorm_bwd.restype = ci
             _lib = L
     return _lib
 
@@ -198,6 +201,12 @@ def glu_add_rmsnorm_fwd(x, x_stride, residual, res_stride, gamma, h, h_stride, y
                         n_rows, n_cols, eps, dtype, stream) -> int:
     return lib().glu_add_rmsnorm_fwd(x, x_stride, residual, res_stride, gamma, h, h_stride, y, y_stride, rstd,
                                      n_rows, n_cols, eps, dtype, stream)
+
+
+def glu_add_rmsnorm_bwd(dy, dy_stride, h, h_stride, rstd, gamma, dh, dh_stride, dx, dx_stride, dres, dres_stride,
+                        dgamma, n_rows, n_cols, dtype, stream) -> int:
+    return lib().glu_add_rmsnorm_bwd(dy, dy_stride, h, h_stride, rstd, gamma, dh, dh_stride, dx, dx_stride, dres,
+                                     dres_stride, dgamma, n_rows, n_cols, dtype, stream)
 
 
 def glu_get_tuning() -> dict:
@@ -381,6 +390,39 @@ def add_rmsnorm(x, residual, gamma, eps: float = 1e-5, *, h=None, y=None, rstd=N
     if st:
         raise GluError(st, "glu_add_rmsnorm_fwd")
     return (h, y, rstd) if want_rstd else (h, y)
+
+
+def add_rmsnorm_bwd(dy, h, rstd, gamma, *, dh=None, dx=None, dres=None, dgamma=None, stream=None):
+    """Gradients of add_rmsnorm: dx (= the residual's gradient) from dy, the
+    stored sum h and rstd, plus dh if h also feeds the residual stream.  ``dres``
+    may be a tensor receiving a second copy; ``dgamma`` a float32 (H,) tensor
+    the row sums are added to, or True for a zeroed one.  Returns dx, or
+    (dx, dgamma) when dgamma is requested."""
+    import torch
+    n_rows, dy_stride = _rows(dy, "dy")
+    _, h_stride = _rows(h, "h")
+    H = dy.shape[-1]
+    if h.shape != dy.shape or h.dtype != dy.dtype:
+        raise ValueError("h must match dy")
+    if gamma.shape != (H,) or gamma.dtype != dy.dtype or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous (H,) tensor of dy's dtype")
+    if rstd.dtype != torch.float32 or rstd.numel() != n_rows or not rstd.is_contiguous():
+        raise ValueError("rstd must be a contiguous float32 tensor with one entry per row")
+    dx = torch.empty_like(dy) if dx is None else dx
+    _, dx_stride = _rows(dx, "dx")
+    dh_ptr, dh_stride = (None, 0) if dh is None else (dh.data_ptr(), _rows(dh, "dh")[1])
+    dr_ptr, dr_stride = (None, 0) if dres is None else (dres.data_ptr(), _rows(dres, "dres")[1])
+    want_dg = dgamma is not None and dgamma is not False
+    if dgamma is True:
+        dgamma = torch.zeros(H, dtype=torch.float32, device=dy.device)
+    if want_dg and (dgamma.dtype != torch.float32 or dgamma.shape != (H,) or not dgamma.is_contiguous()):
+        raise ValueError("dgamma must be a contiguous float32 (H,) tensor")
+    st = glu_add_rmsnorm_bwd(dy.data_ptr(), dy_stride, h.data_ptr(), h_stride, rstd.data_ptr(), gamma.data_ptr(),
+                             dh_ptr, dh_stride, dx.data_ptr(), dx_stride, dr_ptr, dr_stride,
+                             dgamma.data_ptr() if want_dg else None, n_rows, H, _dtype_code(dy), _stream(stream))
+    if st:
+        raise GluError(st, "glu_add_rmsnorm_bwd")
+    return (dx, dgamma) if want_dg else dx
 
 
 # ---- host tensors ---------------------------------------------------------------

@@ -457,6 +457,52 @@ int validate_add_rmsnorm(const void *x, int64_t x_stride, const void *res, int64
     return GLU_OK;
 }
 
+int validate_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void *h, int64_t h_stride, const float *rstd,
+                             const void *gamma, const void *dh, int64_t dh_stride, const void *dx, int64_t dx_stride,
+                             const void *dres, int64_t dres_stride, const float *dgamma, int64_t n_rows,
+                             int64_t n_cols, int dtype, bool *empty)
+{
+    *empty = false;
+    if (!(dtype == GLU_F32 || dtype == GLU_F16 || dtype == GLU_BF16)) return GLU_ERR_ENUM;
+    if (n_rows < 0 || n_cols < 0) return GLU_ERR_SHAPE;
+    if (n_rows == 0 || n_cols == 0) { *empty = true; return GLU_OK; }
+    if (n_cols > kRmsBwdMaxCols) return GLU_ERR_SHAPE;
+    if (!dy || !h || !rstd || !gamma || !dx) return GLU_ERR_NULL;
+    if (n_rows == 1) dy_stride = h_stride = dh_stride = dx_stride = dres_stride = n_cols;
+    if (dy_stride < n_cols || h_stride < n_cols || dx_stride < n_cols || (dh && dh_stride < n_cols) ||
+        (dres && dres_stride < n_cols))
+        return GLU_ERR_STRIDE;
+    const int E = elem_size(dtype);
+    const Mat mdy{uintptr_t(dy), dy_stride, n_cols}, mh{uintptr_t(h), h_stride, n_cols};
+    const Mat mdh{uintptr_t(dh), dh_stride, n_cols}, mdx{uintptr_t(dx), dx_stride, n_cols};
+    const Mat mdr{uintptr_t(dres), dres_stride, n_cols}, mg{uintptr_t(gamma), n_cols, n_cols};
+    if (extent_bytes(mdy, n_rows, E) < 0 || extent_bytes(mh, n_rows, E) < 0 || extent_bytes(mdx, n_rows, E) < 0 ||
+        (dh && extent_bytes(mdh, n_rows, E) < 0) || (dres && extent_bytes(mdr, n_rows, E) < 0) ||
+        extent_bytes(mg, 1, E) < 0)
+        return GLU_ERR_SHAPE;
+    Mat ins[3] = {mdy, mh, mdh}, outs[2] = {mdx, mdr};
+    if (int st = check_aliasing(ins, dh ? 3 : 2, outs, dres ? 2 : 1, n_rows, E)) return st;
+    // small read-only and accumulated vectors: no matrix output may touch them
+    // and they may not touch each other or any matrix
+    const uint64_t gb = uint64_t(n_cols) * E, rb = uint64_t(n_rows) * 4, db = uint64_t(n_cols) * 4;
+    if (uint64_t(n_rows) > (UINTPTR_MAX - uintptr_t(rstd)) / 4) return GLU_ERR_SHAPE;
+    if (dgamma && uint64_t(n_cols) > (UINTPTR_MAX - uintptr_t(dgamma)) / 4) return GLU_ERR_SHAPE;
+    for (int o = 0; o < (dres ? 2 : 1); ++o)
+        if (rows_hit_range(outs[o], n_rows, E, mg.p, gb) || rows_hit_range(outs[o], n_rows, E, uintptr_t(rstd), rb) ||
+            (dgamma && rows_hit_range(outs[o], n_rows, E, uintptr_t(dgamma), db)))
+            return GLU_ERR_ALIAS;
+    if (dgamma) {
+        const Mat all[5] = {mdy, mh, mdh, mdx, mdr};
+        for (int k = 0; k < 5; ++k) {
+            if ((k == 2 && !dh) || (k == 4 && !dres)) continue;
+            if (rows_hit_range(all[k], n_rows, E, uintptr_t(dgamma), db)) return GLU_ERR_ALIAS;
+        }
+        const uint64_t d0 = uintptr_t(dgamma), g0 = mg.p, r0 = uintptr_t(rstd);
+        if (!(d0 + db <= g0 || g0 + gb <= d0) || !(d0 + db <= r0 || r0 + rb <= d0)) return GLU_ERR_ALIAS;
+    }
+    return GLU_OK;
+}
+
 int validate_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_stride, const void *b,
                  int64_t b_stride, const void *da, int64_t da_stride, const void *db,
                  int64_t db_stride, int64_t n_rows, int64_t n_cols, int layout, int act, int dtype,

@@ -94,6 +94,11 @@ constexpr int64_t kRmsMaxCols = 32768;
 int validate_add_rmsnorm(const void *x, int64_t x_stride, const void *res, int64_t res_stride,
                          const void *gamma, const void *h, int64_t h_stride, const void *y, int64_t y_stride,
                          const float *rstd, int64_t n_rows, int64_t n_cols, float eps, int dtype, bool *empty);
+constexpr int64_t kRmsBwdMaxCols = 16384;
+int validate_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void *h, int64_t h_stride, const float *rstd,
+                             const void *gamma, const void *dh, int64_t dh_stride, const void *dx, int64_t dx_stride,
+                             const void *dres, int64_t dres_stride, const float *dgamma, int64_t n_rows,
+                             int64_t n_cols, int dtype, bool *empty);
 
 // One validated call: what the planner needs.  Strides are in elements.
 struct Call {

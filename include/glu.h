@@ -374,6 +374,47 @@ int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride,
                         int64_t n_rows, int64_t n_cols, float eps,
                         glu_dtype_t dtype, glu_stream_t stream);
 
+/*
+ * Backward of glu_add_rmsnorm_fwd ("Skill: Write a Triton Fused Add+RMSNorm
+ * Kernel", Required reasoning process steps 9-10: the forward keeps rstd and
+ * the summed rows h; the gradient of the norm goes to x and to the residual
+ * alike).  For each row, with s = h (the stored sum) and rstd as the forward
+ * kept it:
+ *
+ *     ds[j]     = rstd * gamma[j] * dy[j] - (rstd^3 / H) * s[j] * sum_k gamma[k] dy[k] s[k]
+ *                 (+ dh[j], the gradient reaching h through the residual stream)
+ *     dx[j]     = round(ds[j])            (the gradient of x and of the residual)
+ *     dgamma[j] += sum over rows of dy[j] * s[j] * rstd
+ *
+ * in fp32 (the row sum with fused multiply-adds, reduced over the block).
+ *
+ *   dy, dy_stride        gradient arriving at y.
+ *   h, h_stride          the sums the forward stored.
+ *   rstd                 n_rows floats from the forward.
+ *   gamma                n_cols elements of `dtype`.
+ *   dh, dh_stride        NULL, or the gradient arriving at h.
+ *   dx, dx_stride        output.  May be exactly dy, h or dh (in place).
+ *   dres, dres_stride    NULL, or a second output receiving the same values
+ *                        (the residual's gradient); may be exactly one of the
+ *                        inputs that dx is not.  dx and dres must not overlap.
+ *   dgamma               NULL, or n_cols floats that the row sums are ADDED to
+ *                        (zero it for a fresh gradient).  The additions from
+ *                        different blocks arrive in no fixed order.
+ *   n_cols               at most 16384, else GLU_ERR_SHAPE.
+ * Other rules as glu_add_rmsnorm_fwd (device pointers, element strides,
+ * GLU_ERR_ALIAS for any other overlap, asynchronous on `stream`).
+ */
+int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride,
+                        const void *h, int64_t h_stride,
+                        const float *rstd,
+                        const void *gamma,
+                        const void *dh, int64_t dh_stride,
+                        void *dx, int64_t dx_stride,
+                        void *dres, int64_t dres_stride,
+                        float *dgamma,
+                        int64_t n_rows, int64_t n_cols,
+                        glu_dtype_t dtype, glu_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -311,3 +311,33 @@ def test_add_rmsnorm_valid_calls_reach_the_cuda_runtime_without_a_gpu():
     assert rms(h=BASE, y=BASE + (1 << 20)) == CUDA        # h over x, y over the residual
     assert rms(h=BASE + (1 << 20), y=BASE, rstd=None) == CUDA
     assert rms(x=BASE + 2, sx=67, cols=61) == CUDA        # unaligned: element accesses
+
+
+def rmsb(dy=BASE, sdy=64, h=BASE + (1 << 20), sh=64, rstd=BASE + (2 << 20), g=BASE + (3 << 20),
+         dh=None, sdh=0, dx=BASE + (4 << 20), sdx=64, dres=None, sdr=0, dg=BASE + (5 << 20), rows=4, cols=64,
+         dtype=BF16):
+    return glu.glu_add_rmsnorm_bwd(dy, sdy, h, sh, rstd, g, dh, sdh, dx, sdx, dres, sdr, dg, rows, cols, dtype, None)
+
+
+@cpu_only
+def test_add_rmsnorm_bwd_validation():
+    assert rmsb(dtype=5) == ENUM
+    assert rmsb(rows=-1) == SHAPE and rmsb(cols=16385, sdy=16400, sh=16400, sdx=16400) == SHAPE
+    assert rmsb(dy=None, h=None, rstd=None, g=None, dx=None, dg=None, rows=0) == OK
+    for k in ("dy", "h", "rstd", "g", "dx"):
+        assert rmsb(**{k: None}) == NULL, k
+    assert rmsb(sdy=63) == STRIDE and rmsb(sdx=1) == STRIDE
+    assert rmsb(dh=BASE + (6 << 20), sdh=3) == STRIDE and rmsb(dres=BASE + (7 << 20), sdr=5) == STRIDE
+    assert rmsb(dx=BASE + 4) == ALIAS                                     # dx shifted over dy
+    assert rmsb(dres=BASE + (4 << 20), sdr=64) == ALIAS                   # dres on dx
+    assert rmsb(dx=BASE + (3 << 20) + 2) == ALIAS                         # dx over gamma
+    assert rmsb(dx=BASE + (2 << 20)) == ALIAS                             # dx over rstd
+    assert rmsb(dg=BASE + 100) == ALIAS and rmsb(dg=BASE + (3 << 20) + 4) == ALIAS
+    assert rmsb(dg=BASE + (2 << 20) + 8) == ALIAS                         # dgamma over rstd
+
+
+@cpu_only
+def test_add_rmsnorm_bwd_valid_calls_reach_the_cuda_runtime_without_a_gpu():
+    assert rmsb() == CUDA
+    assert rmsb(dx=BASE, dres=BASE + (1 << 20), sdr=64, dg=None) == CUDA      # in place over dy and h
+    assert rmsb(dh=BASE + (6 << 20), sdh=64, dx=BASE + (6 << 20)) == CUDA    # in place over dh

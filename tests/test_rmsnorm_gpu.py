@@ -166,3 +166,118 @@ def test_decoder_block_workload(orc):
     d = glu_synth.add_rmsnorm()
     h, y, rstd = run(d["x"], d["res"], d["gamma"], "bf16", d["eps"])
     check(orc, "bf16", d["x"], d["res"], d["gamma"], d["eps"], h, y, rstd, "decoder block")
+
+
+# ---------------------------------------------------------------- backward
+# ds (dx, dres) against the oracle's exact value: the fp32 path may differ by
+# E = 32 * 2^-24 * (|rstd gamma dy| + rstd^3 / H * sum_k |gamma dy s| * |s| + |dh|)
+# (the row sum carries at most 21 roundings of its terms' magnitudes, rstd^3/H a
+# few more, each product and sum one), then one rounding into the dtype.
+# dgamma: one fused multiply-add per row per block and one atomic addition per
+# block, at most (rows + blocks) roundings of sum_r |dy s rstd|.
+
+U = 2.0 ** -24
+
+
+def ulp(dt, v):
+    v = np.abs(np.asarray(v, dtype=np.float64))
+    lo, p = {"bf16": (-126, 7), "f16": (-14, 10), "f32": (-126, 23)}[dt]
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** lo)))
+    return 2.0 ** (np.maximum(e, lo) - p)
+
+
+def bwd_inputs(rows, H, dt, seed, with_dh):
+    rng = np.random.default_rng([seed, rows, H, DTYPES.index(dt), int(with_dh)])
+    h = glu_synth.normal_bits(rng, (rows, H), 3.0, dt)
+    dy = glu_synth.normal_bits(rng, (rows, H), 1.0, dt)
+    g = glu_synth.f32_to_bits(rng.standard_normal(H, dtype=np.float32) * np.float32(0.2) + np.float32(1.0), dt)
+    rstd = (rng.random(rows, dtype=np.float32) * np.float32(0.5) + np.float32(0.2)).astype(np.float32)
+    dh = glu_synth.normal_bits(rng, (rows, H), 0.5, dt) if with_dh else None
+    return dy, h, rstd, g, dh
+
+
+def check_bwd(orc, dt, dy, h, rstd, g, dh, dx_gpu, dg_gpu, what, n_blocks=5000):
+    _, ds, dgamma = orc.add_rmsnorm_bwd(dt, dy, h, rstd, g, dh)
+    d, s, gv = orc.decode(dt, dy), orc.decode(dt, h), orc.decode(dt, g)
+    rs = rstd.astype(np.float64)[:, None]
+    H = d.shape[1]
+    big = np.sum(np.abs(gv[None, :] * d * s), axis=1, keepdims=True)
+    E = 32 * U * (np.abs(rs * gv[None, :] * d) + rs ** 3 / H * big * np.abs(s) +
+                  (np.abs(orc.decode(dt, dh)) if dh is not None else 0.0))
+    got = orc.decode(dt, dx_gpu)
+    allow = E + ulp(dt, np.abs(ds) + E)
+    bad = np.flatnonzero(~(np.abs(got - ds) <= allow))
+    assert bad.size == 0, (f"{what}: {bad.size} ds outside the bound; first {bad[0]}: gpu {got.ravel()[bad[0]]!r} "
+                           f"exact {ds.ravel()[bad[0]]!r} allow {allow.ravel()[bad[0]]!r}")
+    if dg_gpu is not None:
+        rows = d.shape[0]
+        scale = np.sum(np.abs(d * s * rs), axis=0)
+        err = np.abs(dg_gpu.astype(np.float64) - dgamma)
+        assert np.all(err <= (rows + n_blocks) * U * scale + 1e-30), f"{what}: dgamma off by {err.max():.3g}"
+
+
+def run_bwd(dy, h, rstd, g, dh, dt, dres=False, dgamma=True):
+    dyd, hd, gd = to_dev(dy, dt), to_dev(h, dt), to_dev(g, dt)
+    rd = torch.from_numpy(rstd).cuda()
+    dhd = to_dev(dh, dt) if dh is not None else None
+    dr = torch.empty_like(dyd) if dres else None
+    out = glu.add_rmsnorm_bwd(dyd, hd, rd, gd, dh=dhd, dres=dr, dgamma=True if dgamma else None)
+    torch.cuda.synchronize()
+    dx, dg = out if dgamma else (out, None)
+    if dres:
+        assert torch.equal(dr.view(TORCH_INT_OF[dt]), dx.view(TORCH_INT_OF[dt]))
+    return to_bits(dx, dt), (dg.cpu().numpy() if dg is not None else None)
+
+
+TORCH_INT_OF = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}
+BWD_SHAPES = [(1, 1), (3, 7), (5, 64), (77, 100), (33, 1000), (64, 4096), (9, 5000), (17, 8192), (4, 16384),
+              (513, 1536)]
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", BWD_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_parity(orc, shape, dt):
+    rows, H = shape
+    for with_dh, dres in ((False, False), (True, True)):
+        dy, h, rstd, g, dh = bwd_inputs(rows, H, dt, 20, with_dh)
+        dx, dg = run_bwd(dy, h, rstd, g, dh, dt, dres=dres)
+        info = glu.glu_last_launch()
+        E = 4 if dt == "f32" else 2
+        vec = (H * E) % 16 == 0 and H <= 1024 * (32 // E)
+        assert info["backward"] == 1 and info["vec_bytes"] == (16 if vec else E) and info["grid"] <= rows
+        check_bwd(orc, dt, dy, h, rstd, g, dh, dx, dg, f"bwd {dt} {shape} dh={with_dh}")
+
+
+@pytest.mark.parametrize("dt", ("bf16", "f32"))
+def test_bwd_in_place_and_accumulation(orc, dt):
+    """dx over dy and dres over h; then dx over dh; dgamma adds to what it holds."""
+    rows, H = 300, 2048
+    dy, h, rstd, g, dh = bwd_inputs(rows, H, dt, 21, True)
+    dyd, hd, gd, dhd = to_dev(dy, dt), to_dev(h, dt), to_dev(g, dt), to_dev(dh, dt)
+    rd = torch.from_numpy(rstd).cuda()
+    dg = torch.zeros(H, dtype=torch.float32, device="cuda")
+    glu.add_rmsnorm_bwd(dyd, hd, rd, gd, dh=dhd, dx=dyd, dres=hd, dgamma=dg)
+    torch.cuda.synchronize()
+    check_bwd(orc, dt, dy, h, rstd, g, dh, to_bits(dyd, dt), dg.cpu().numpy(), "in place over dy")
+    assert torch.equal(dyd.view(TORCH_INT_OF[dt]), hd.view(TORCH_INT_OF[dt]))
+    # a second call over the untouched originals, dx over dh, adds the same dgamma again
+    dyd, hd, dhd = to_dev(dy, dt), to_dev(h, dt), to_dev(dh, dt)
+    glu.add_rmsnorm_bwd(dyd, hd, rd, gd, dh=dhd, dx=dhd, dgamma=dg)
+    torch.cuda.synchronize()
+    check_bwd(orc, dt, dy, h, rstd, g, dh, to_bits(dhd, dt), dg.cpu().numpy() / 2, "in place over dh")
+
+
+def test_forward_then_backward_decoder_block(orc):
+    """The training step's pair on the decoder-block workload: the forward's h
+    and rstd feed the backward; every element against the oracle given the same
+    h and rstd."""
+    d = glu_synth.add_rmsnorm()
+    rows, H = d["x"].shape
+    xd, rd_, gd = to_dev(d["x"], "bf16"), to_dev(d["res"], "bf16"), to_dev(d["gamma"], "bf16")
+    h, y, rstd = glu.add_rmsnorm(xd, rd_, gd, d["eps"], rstd=True)
+    rng = np.random.default_rng(22)
+    dy = glu_synth.normal_bits(rng, (rows, H), 1.0, "bf16")
+    dx, dg = glu.add_rmsnorm_bwd(to_dev(dy, "bf16"), h, rstd, gd, dgamma=True)
+    torch.cuda.synchronize()
+    check_bwd(orc, "bf16", dy, to_bits(h, "bf16"), rstd.cpu().numpy(), d["gamma"], None, to_bits(dx, "bf16"),
+              dg.cpu().numpy(), "decoder block backward")
