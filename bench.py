@@ -58,8 +58,10 @@ def config(extra=None):
     return c
 
 
-# the sources the streaming kernels and their launch plan are built from
-STREAMING_SOURCES = ("glu_api.cu", "glu_inst_bf16.cu", "glu_kernels.cuh", "glu_math.cuh", "glu_plan.h")
+# the sources the streaming kernels are compiled from; their launch shape is
+# compared separately (ncu_traffic)
+STREAMING_SOURCES = ("glu_inst_bf16.cu", "glu_kernels.cuh", "glu_math.cuh", "glu_plan.h")
+LAUNCH_KEYS = ("vec_bytes", "unroll", "threads", "grid", "flattened", "path")
 
 
 def source_sha() -> str:
@@ -79,15 +81,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic():
+def ncu_traffic(launch_bwd=None):
     """Per-launch DRAM bytes of the backward kernel from the committed ncu
-    summary, or None if the kernel sources changed since it was taken."""
+    summary, or None if the kernel sources or its launch shape changed since
+    it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
     if t.get("source_sha") != source_sha():
+        return None
+    rec = t.get("bwd_launch")
+    if launch_bwd is not None and rec is not None and any(rec.get(k) != launch_bwd.get(k) for k in LAUNCH_KEYS):
         return None
     return t.get("bwd_dram_bytes_per_launch")
 
@@ -320,7 +326,7 @@ def run_gpu(args, rank, world, local_rank):
     bwd_avg = statistics.fmean(bwd_ms)
     fwd_avg = statistics.fmean(fwd_ms)
     achieved = BWD_BYTES / (bwd_avg * 1e-3) / 1e9
-    traffic = ncu_traffic()
+    traffic = ncu_traffic(launch_bwd)
     value = job_gbs(world, K, STEP_BYTES, total_ms)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,

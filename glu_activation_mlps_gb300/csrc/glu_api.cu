@@ -9,7 +9,7 @@
 #include <cstring>
 
 #include "glu.h"
-#include "glu_plan.h"
+#include "glu_internal.h"
 
 namespace {
 

@@ -15,6 +15,7 @@
 // issued, and returns, so no block can hang the GPU.
 // Included by glu_bulk.cu only.
 #pragma once
+#include "glu_internal.h"
 #include "glu_kernels.cuh"
 
 namespace glu {

@@ -11,7 +11,7 @@
 #include <cstdio>
 
 #include "glu.h"
-#include "glu_plan.h"
+#include "glu_internal.h"
 
 namespace {
 

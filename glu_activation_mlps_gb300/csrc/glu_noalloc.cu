@@ -25,7 +25,7 @@
 #include <mutex>
 
 #include "glu.h"
-#include "glu_plan.h"
+#include "glu_internal.h"
 
 namespace {
 

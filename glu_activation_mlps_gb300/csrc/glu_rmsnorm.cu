@@ -29,7 +29,7 @@
 
 #include "glu.h"
 #include "glu_kernels.cuh"
-#include "glu_plan.h"
+#include "glu_internal.h"
 
 namespace glu {
 namespace rms {
