@@ -15,6 +15,7 @@ from torch import nn
 
 from . import bwd as _bwd
 from . import fwd as _fwd
+from . import gemm_fwd as _gemm_fwd
 
 ACTS = ("silu", "gelu_erf", "gelu_tanh", "relu")
 
@@ -93,12 +94,35 @@ class GLU(nn.Module):
         return f"act={self.act}, inplace_backward={self.inplace_backward}"
 
 
+def _gemm_ready(x, w) -> bool:
+    """Inputs the tensor-core GEMM with the activation in its epilogue takes:
+    f16/bf16 CUDA tensors of one dtype, rows contiguous, 16-byte aligned bases
+    and row strides (the tensor-memory accelerator's rule)."""
+    if not (x.is_cuda and x.dtype in (torch.float16, torch.bfloat16) and w.dtype == x.dtype):
+        return False
+    if x.stride(-1) != 1 or w.stride(-1) != 1 or x.data_ptr() % 16 or w.data_ptr() % 16:
+        return False
+    if (w.stride(0) * w.element_size()) % 16:
+        return False
+    if x.dim() > 1 and (x.stride(-2) * x.element_size()) % 16:
+        return False
+    return True
+
+
 class GatedMLP(nn.Module):
     """down(act(x W_gate^T) * (x W_up^T)) with the projections as torch Linear
     layers (no bias) and the gated activation from the library.  With
     ``fused_gate_up`` the gate and up projections are one Linear of 2 * I
     outputs whose result feeds the [gate | up] layout directly, so no split or
-    copy is needed between the projection and the activation."""
+    copy is needed between the projection and the activation.
+
+    Without autograd (inference: torch.no_grad(), or no input or weight that
+    requires a gradient) the gate and up projections and the activation run
+    as one tensor-core GEMM with the activation in its epilogue (glu_gemm_fwd),
+    so the gate and up matrices never reach HBM ("Skill: Write a Triton
+    SiLU-Mul (SwiGLU) Kernel", Performance requirements, "Versus epilogue
+    fusion").  Training keeps the projections, because the backward needs
+    them."""
 
     def __init__(self, hidden: int, intermediate: int, act: str = "silu", fused_gate_up: bool = True,
                  device=None, dtype=None):
@@ -113,7 +137,18 @@ class GatedMLP(nn.Module):
             self.up_proj = nn.Linear(hidden, intermediate, **kw)
         self.down_proj = nn.Linear(intermediate, hidden, **kw)
 
+    def _gate_up_weights(self):
+        if self.fused_gate_up:
+            w = self.gate_up_proj.weight
+            n = w.shape[0] // 2
+            return w[:n], w[n:]
+        return self.gate_proj.weight, self.up_proj.weight
+
     def forward(self, x):
+        wg, wu = self._gate_up_weights()
+        grad = torch.is_grad_enabled() and (x.requires_grad or wg.requires_grad or wu.requires_grad)
+        if not grad and _gemm_ready(x, wg) and _gemm_ready(x, wu) and wg.stride(0) == wu.stride(0):
+            return self.down_proj(_gemm_fwd(x, wg, wu, act=self.act))
         if self.fused_gate_up:
             h = glu(self.gate_up_proj(x), act=self.act, inplace_backward=True)
         else:

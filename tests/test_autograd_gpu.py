@@ -97,3 +97,22 @@ def test_gated_mlp_matches_plain_torch(fused):
     yr.backward(gy)
     assert torch.allclose(x.grad.float(), xr.grad.float(), atol=3e-2, rtol=3e-2)
     assert mlp.down_proj.weight.grad is not None
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_gated_mlp_inference_uses_the_fused_gemm(fused, act):
+    """Under torch.no_grad() the module runs glu_gemm_fwd (the last launch is the
+    GEMM's) and agrees with its training path on the same weights."""
+    torch.manual_seed(1)
+    hidden, inter = 512, 1408
+    mlp = ga.GatedMLP(hidden, inter, act=act, fused_gate_up=fused, device="cuda", dtype=torch.bfloat16)
+    x = torch.randn(3, 70, hidden, device="cuda", dtype=torch.bfloat16)
+    y_train = mlp(x.clone().requires_grad_(True)).detach()
+    wg, wu = mlp._gate_up_weights()
+    with torch.no_grad():
+        h = glu.gemm_fwd(x, wg, wu, act=act)
+        assert glu.glu_last_launch()["path"] == 3
+        y = mlp(x)
+    assert torch.equal(y, mlp.down_proj(h).detach())
+    assert torch.allclose(y.float(), y_train.float(), atol=2e-2, rtol=2e-2)
