@@ -22,7 +22,10 @@
  *   - All pointers are DEVICE pointers into memory the caller owns.  The
  *     library allocates nothing, keeps no pointer after the call returns, and
  *     is asynchronous: work is enqueued on `stream` (NULL = the legacy default
- *     stream) and the call returns before it runs.
+ *     stream) and the call returns before it runs.  Pinned host memory
+ *     (cudaHostAlloc, cudaHostRegister) is device memory in this sense: the
+ *     kernels then read and write it in place over the host link (zero-copy),
+ *     except glu_gemm_fwd, whose operands must be in device memory.
  *   - Matrices are row-major with a contiguous last dimension: element (r, c)
  *     of operand X is at X + r * X_stride + c.  Strides are in ELEMENTS of
  *     `dtype`, not bytes, and are ignored when n_rows == 1.
@@ -97,7 +100,8 @@ typedef enum {
     GLU_ERR_ENUM = -5,    /* unknown act, layout or dtype */
     GLU_ERR_CUDA = -6,    /* the CUDA runtime refused a launch or copy; see glu_last_cuda_error() */
     GLU_ERR_WORKSPACE = -7, /* host-memory entry points: workspace NULL or too small for one row */
-    GLU_ERR_VALUE = -8      /* a numeric argument out of range (glu_add_rmsnorm_fwd: eps) */
+    GLU_ERR_VALUE = -8      /* an argument out of range: glu_add_rmsnorm_fwd's eps, or an
+                               operand of glu_gemm_fwd that is not in device memory */
 } glu_status_t;
 
 /*
@@ -324,8 +328,9 @@ int glu_wait_timeouts(unsigned int *count, int reset);
  * must be 16-byte aligned and x_stride, w_stride multiples of 8 elements,
  * else GLU_ERR_STRIDE (y has no alignment rule).  M, K, I < 2^31.  M == 0 or
  * I == 0 returns GLU_OK without work; K == 0 sets y to 0 (act(0) * 0).
- * All pointers are device pointers; the library keeps none after the call.
- * A wait that runs out of its time budget (about a second) is counted for
+ * All pointers must be device memory (cudaMalloc and the like; checked with
+ * cudaPointerGetAttributes, else GLU_ERR_VALUE); the library keeps none after
+ * the call.  A wait that runs out of its time budget (about a second) is counted for
  * glu_wait_timeouts() and leaves that block's outputs unwritten.
  * Returns GLU_OK or a negative glu_status_t.
  */

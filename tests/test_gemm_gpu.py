@@ -268,3 +268,18 @@ def test_full_layer_sampled(orc, exact):
     else:
         check_bound(orc, "silu", "bf16", yb, g, u, sg, su, K, "full layer normal")
     assert not torch.isnan(y).any()
+
+
+def test_host_memory_operands_are_refused():
+    """The tensor-memory accelerator path takes device memory only: a pinned
+    host operand is refused before any launch (GLU_ERR_VALUE)."""
+    x = torch.zeros(128, 64, dtype=torch.bfloat16).pin_memory()
+    w = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = glu.glu_gemm_fwd(x.data_ptr(), 64, w.data_ptr(), w.data_ptr(), 64, y.data_ptr(), 64, 128, 64, 64, 0, 2, s)
+    assert st == -8
+    yh = torch.zeros(128, 64, dtype=torch.bfloat16).pin_memory()
+    xd = x.cuda()
+    st = glu.glu_gemm_fwd(xd.data_ptr(), 64, w.data_ptr(), w.data_ptr(), 64, yh.data_ptr(), 64, 128, 64, 64, 0, 2, s)
+    assert st == -8

@@ -9,6 +9,7 @@ import torch
 
 import glu_activation_mlps_gb300 as glu
 import glu_synth
+import helpers
 from helpers import compare
 
 pytestmark = pytest.mark.gpu
@@ -122,3 +123,30 @@ def test_host_metric_workload_sampled(orc):
     da_o, db_o = orc.bwd("silu", "bf16", dc_s, a_s, b_s)
     compare(bits_of(da, "bf16").ravel()[idx], da_o, "bf16", what="metric host da")
     compare(bits_of(db, "bf16").ravel()[idx], db_o, "bf16", what="metric host db")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_device_entry_points_on_pinned_host_memory(orc, dt):
+    """glu_fwd / glu_bwd on pinned host buffers (the kernels read and write them
+    in place over the host link): element by element against the oracle."""
+    rows, cols = 300, 2000
+    rng = np.random.default_rng(77)
+    a = glu_synth.normal_bits(rng, (rows, cols), 2.0, dt)
+    b = glu_synth.normal_bits(rng, (rows, cols), 1.0, dt)
+    dc = glu_synth.normal_bits(rng, (rows, cols), 1.0, dt)
+    T = helpers.TORCH[dt]
+    pin = lambda bits: torch.from_numpy(bits.view(helpers.NP_SIGNED[dt])).view(T).pin_memory()
+    A, B, DC = pin(a), pin(b), pin(dc)
+    Y, DA, DB = (torch.empty(rows, cols, dtype=T).pin_memory() for _ in range(3))
+    s = torch.cuda.current_stream().cuda_stream
+    code = {"bf16": 2, "f32": 0}[dt]
+    assert glu.glu_fwd(A.data_ptr(), cols, B.data_ptr(), cols, Y.data_ptr(), cols, rows, cols, 0, 0, code, s) == 0
+    assert glu.glu_bwd(DC.data_ptr(), cols, A.data_ptr(), cols, B.data_ptr(), cols, DA.data_ptr(), cols,
+                       DB.data_ptr(), cols, rows, cols, 0, 0, code, s) == 0
+    torch.cuda.synchronize()
+    bits = lambda t: t.view(helpers.TORCH_INT[dt]).numpy().view(helpers.NP_BITS[dt])
+    helpers.compare(bits(Y), orc.fwd("silu", dt, a, b), dt, what="zero-copy y")
+    da, db = orc.bwd("silu", dt, dc, a, b)
+    scale = orc.bwd_da_scale("silu", dt, dc, a, b) if dt == "f32" else None
+    helpers.compare(bits(DA), da, dt, scale=scale, what="zero-copy da")
+    helpers.compare(bits(DB), db, dt, what="zero-copy db")
