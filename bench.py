@@ -476,6 +476,56 @@ def run_table(args):
             for act in glu_synth.SWEEP_ACTS:
                 for d in ("fwd", "bwd"):
                     split_case("sweep", 4096, H, dt, act, d)
+    # context: the same forward and backward as plain PyTorch (eager, and
+    # torch.compile where it works on this machine) at the metric shape
+    cmp = []
+    A = torch.randn(ROWS, COLS, device="cuda", generator=gen).to(torch.bfloat16)
+    B = torch.randn(ROWS, COLS, device="cuda", generator=gen).to(torch.bfloat16)
+    DC = torch.randn(ROWS, COLS, device="cuda", generator=gen).to(torch.bfloat16)
+
+    def t_fwd(a, b):
+        return torch.nn.functional.silu(a.float()).mul(b.float()).to(a.dtype)
+
+    def t_bwd(dc, a, b):
+        af, bf, cf = a.float(), b.float(), dc.float()
+        sg = torch.sigmoid(af)
+        silu = af * sg
+        return (cf * (silu * (1 - sg) + sg) * bf).to(a.dtype), (cf * silu).to(a.dtype)
+
+    def once(fn, reps=20):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    Y0, Y1 = torch.empty_like(A), torch.empty_like(A)
+
+    def ours_fwd():
+        assert L.glu_fwd(A.data_ptr(), COLS, B.data_ptr(), COLS, Y0.data_ptr(), COLS, ROWS, COLS, 0, 0, 2, s) == 0
+
+    def ours_bwd():
+        assert L.glu_bwd(DC.data_ptr(), COLS, A.data_ptr(), COLS, B.data_ptr(), COLS, Y0.data_ptr(), COLS,
+                         Y1.data_ptr(), COLS, ROWS, COLS, 0, 0, 2, s) == 0
+
+    cmp.append(("fwd", once(ours_fwd), once(lambda: t_fwd(A, B))))
+    cmp.append(("bwd", once(ours_bwd), once(lambda: t_bwd(DC, A, B))))
+    try:
+        cf, cb = torch.compile(t_fwd), torch.compile(t_bwd)
+        compiled = [once(lambda: cf(A, B)), once(lambda: cb(DC, A, B))]
+    except Exception as exc:       # no compiler toolchain on the GPU machine: report why
+        compiled = [f"unavailable ({type(exc).__name__})"] * 2
+    print("| SwiGLU bf16 4096x14336 | this library (us) | torch eager (us) | torch.compile (us) |")
+    print("|---|---|---|---|")
+    for (d, ours, eager), comp in zip(cmp, compiled):
+        comp_s = f"{comp:.1f}" if isinstance(comp, float) else comp
+        print(f"| {d} | {ours:.1f} | {eager:.1f} | {comp_s} |", flush=True)
+    print()
     print(f"| workload | shape | dtype | act | dir | us / launch | GB/s | % of {peak:.0f} GB/s ({src}) |")
     print("|---|---|---|---|---|---|---|---|")
     for name, shape, dt, act, d, us, gbs in rows:
