@@ -13,6 +13,8 @@ from __future__ import annotations
 import torch
 from torch import nn
 
+from . import add_rmsnorm as _add_rmsnorm
+from . import add_rmsnorm_bwd as _add_rmsnorm_bwd
 from . import bwd as _bwd
 from . import fwd as _fwd
 from . import gemm_fwd as _gemm_fwd
@@ -154,3 +156,46 @@ class GatedMLP(nn.Module):
         else:
             h = glu(self.gate_proj(x), self.up_proj(x), act=self.act, inplace_backward=True)
         return self.down_proj(h)
+
+
+class AddRMSNormFunction(torch.autograd.Function):
+    """(h, y) = (x + residual, rmsnorm(x + residual) * gamma) in one pass
+    ("Skill: Write a Triton Fused Add+RMSNorm Kernel", Purpose; steps 9-10 for
+    the backward).  The forward saves h and rstd; the backward sends the same
+    gradient to x and to the residual (the norm's gradient plus the gradient
+    arriving at h from the residual stream) and accumulates gamma's."""
+
+    @staticmethod
+    def forward(ctx, x, residual, gamma, eps: float = 1e-5):
+        h, y, rstd = _add_rmsnorm(x, residual, gamma, eps, rstd=True)
+        ctx.save_for_backward(h, rstd, gamma)
+        return h, y
+
+    @staticmethod
+    def backward(ctx, dh, dy):
+        h, rstd, gamma = ctx.saved_tensors
+        if dy is None:
+            dy = torch.zeros_like(h)
+        dy = dy if dy.stride(-1) == 1 else dy.contiguous()
+        if dh is not None and dh.stride(-1) != 1:
+            dh = dh.contiguous()
+        want_g = ctx.needs_input_grad[2]
+        out = _add_rmsnorm_bwd(dy, h, rstd, gamma, dh=dh, dgamma=True if want_g else None)
+        dx, dg = out if want_g else (out, None)
+        return dx, dx, (dg.to(gamma.dtype) if dg is not None else None), None
+
+
+class FusedAddRMSNorm(nn.Module):
+    """The residual add + RMSNorm at the end of a decoder sub-block:
+    forward(x, residual) -> (h, y), h the next block's residual stream."""
+
+    def __init__(self, hidden: int, eps: float = 1e-5, device=None, dtype=None):
+        super().__init__()
+        self.eps = eps
+        self.weight = nn.Parameter(torch.ones(hidden, device=device, dtype=dtype))
+
+    def forward(self, x, residual):
+        return AddRMSNormFunction.apply(x, residual, self.weight, self.eps)
+
+    def extra_repr(self):
+        return f"{self.weight.shape[0]}, eps={self.eps}"

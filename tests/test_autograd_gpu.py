@@ -116,3 +116,33 @@ def test_gated_mlp_inference_uses_the_fused_gemm(fused, act):
         y = mlp(x)
     assert torch.equal(y, mlp.down_proj(h).detach())
     assert torch.allclose(y.float(), y_train.float(), atol=2e-2, rtol=2e-2)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_fused_add_rmsnorm_module_matches_torch_autograd(dt):
+    """FusedAddRMSNorm against torch autograd through x + residual and F.rms_norm,
+    with gradients arriving at both outputs (y, and h through the residual stream)."""
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    torch.manual_seed(3)
+    H = 1536
+    mod = ga.FusedAddRMSNorm(H, eps=1e-5, device="cuda", dtype=dt)
+    with torch.no_grad():
+        mod.weight.copy_(1 + 0.1 * torch.randn(H, device="cuda"))
+    x = torch.randn(4, 50, H, device="cuda", dtype=dt, requires_grad=True)
+    r = (4 * torch.randn(4, 50, H, device="cuda")).to(dt).requires_grad_(True)
+    h, y = mod(x, r)
+    gh, gy = torch.randn_like(h), torch.randn_like(y)
+    (h * gh).sum().backward(retain_graph=True)
+    (y * gy).sum().backward()
+    xr = x.detach().double().requires_grad_(True)
+    rr = r.detach().double().requires_grad_(True)
+    wr = mod.weight.detach().double().requires_grad_(True)
+    hr = xr + rr
+    yr = F.rms_norm(hr, (H,), wr, 1e-5)
+    ((hr * gh.double()).sum() + (yr * gy.double()).sum()).backward()
+    tol = 2e-2 if dt == torch.bfloat16 else 1e-4
+    assert torch.allclose(y.double(), yr, atol=tol, rtol=tol)
+    assert torch.allclose(x.grad.double(), xr.grad, atol=tol, rtol=tol)
+    assert torch.allclose(r.grad.double(), rr.grad, atol=tol, rtol=tol)
+    assert torch.allclose(mod.weight.grad.double(), wr.grad, atol=tol * 50, rtol=tol)
