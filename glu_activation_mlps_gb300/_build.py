@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libglu_gb300.so")
 
 SOURCES = ["glu_api.cu", "glu_host.cu", "glu_noalloc.cu", "glu_bulk.cu", "glu_inst_bf16.cu",
            "glu_inst_f16.cu", "glu_inst_f32.cu", "glu_gemm.cu", "glu_rmsnorm.cu"]
-HEADERS = ["glu_plan.h", "glu_internal.h", "glu_math.cuh", "glu_kernels.cuh", "glu_bulk.cuh"]
+HEADERS = ["glu_plan.h", "glu_internal.h", "glu_math.cuh", "glu_kernels.cuh", "glu_bulk.cuh", "glu_async.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -614,11 +614,12 @@ int glu_version(void) { return GLU_VERSION; }
 int glu_wait_timeouts(unsigned int *count, int reset)
 {
     if (!count) return GLU_ERR_NULL;
-    unsigned int bulk = 0, gemm = 0;
+    unsigned int bulk = 0, gemm = 0, rms = 0;
     cudaError_t e = glu::bulk_timeouts(&bulk, reset != 0);
     if (e == cudaSuccess) e = glu::gemm::timeouts(&gemm, reset != 0);
+    if (e == cudaSuccess) e = glu::rms::timeouts(&rms, reset != 0);
     if (e != cudaSuccess) return cuda_fail(e);
-    *count = bulk + gemm;
+    *count = bulk + gemm + rms;
     return GLU_OK;
 }
 

@@ -15,6 +15,7 @@
 // issued, and returns, so no block can hang the GPU.
 // Included by glu_bulk.cu only.
 #pragma once
+#include "glu_async.cuh"
 #include "glu_internal.h"
 #include "glu_kernels.cuh"
 
@@ -22,7 +23,6 @@ namespace glu {
 
 constexpr int kBulkChunk = 16384;                       // bytes per operand per stage
 static_assert(kBulkChunk == kBulkChunkHost, "host view of the bulk chunk");
-constexpr long long kWaitBudgetCycles = 2000000000LL;   // ~1 s at 2 GHz
 
 // Two shapes: WIDE = one block per SM with 8 consumer warps and a 192 KiB
 // ring; NARROW = two blocks per SM, each with 16 consumer warps and a 96 KiB
@@ -42,53 +42,6 @@ struct BulkShape {
 
 // Waits that ran out, summed over all bulk launches since the last reset.
 static __device__ unsigned int g_bulk_timeouts;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Waits for the phase with the given parity to complete; false if the clock
-// budget ran out first.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (true) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (clock64() - t0 > kWaitBudgetCycles) return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
 
 template <class Act, class T, int DIR, bool NARROW>
 __global__ void __launch_bounds__(BulkShape<DIR, NARROW>::kThreads, NARROW ? 2 : 1)

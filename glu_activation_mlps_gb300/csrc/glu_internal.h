@@ -28,6 +28,9 @@ cudaError_t bulk_timeouts(unsigned int *count, bool reset);
 namespace gemm {
 cudaError_t timeouts(unsigned int *count, bool reset);   // glu_gemm.cu
 }
+namespace rms {
+cudaError_t timeouts(unsigned int *count, bool reset);   // glu_rmsnorm.cu
+}
 void record_launch(const glu_launch_info_t &info);       // this thread's glu_last_launch
 
 // Fused residual add + RMSNorm (glu_rmsnorm.cu): argument rules shared with glu_api.cu.

@@ -28,6 +28,7 @@
 #include <cstdint>
 
 #include "glu.h"
+#include "glu_async.cuh"
 #include "glu_kernels.cuh"
 #include "glu_internal.h"
 
@@ -321,7 +322,11 @@ struct BwdParams {
     int H;
     int tpr;                            // threads per row (a multiple of 32)
     int groups;                         // rows a block works on at once
+    int stages;                         // staged kernel: shared-memory ring depth, in row groups
 };
+
+// Waits of the staged backward that ran out, summed since the last reset.
+static __device__ unsigned int g_rms_timeouts;
 
 __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
 {
@@ -330,76 +335,405 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
                  : "memory");
 }
 
+// The sum of v over the tpr threads of one row group; every thread of the
+// group gets it.  `r` holds 33 floats, alternating between two arrays on
+// consecutive rows like block_sum.  Warp sums, one barrier, then each thread
+// adds its group's warp sums in order; for groups of more than 8 warps the
+// group's first warp adds them and a second barrier shares the result.
+__device__ __forceinline__ float group_sum(float v, float *r, int lane, int wig, int nwg)
+{
+    v = warp_sum(v);
+    if (lane == 0) r[wig] = v;
+    __syncthreads();
+    if (nwg <= 8) {
+        float t = 0.0f;
+        for (int w = 0; w < nwg; ++w) t += r[w];
+        return t;
+    }
+    if (wig == 0) {
+        float t = lane < nwg ? r[lane] : 0.0f;
+        t = warp_sum(t);
+        if (lane == 0) r[32] = t;
+    }
+    __syncthreads();
+    return r[32];
+}
+
+// Adds each thread's dgamma partial sums (dg[k], column col(k)) to dgamma:
+// with one row per block straight from registers, 16-byte reductions where
+// dgamma is 16-byte aligned; with several rows per block the groups first add
+// theirs in the shared array dgs (H floats), then the block adds dgs once, so
+// global additions number about blocks x H / 4.  Called by every thread of
+// the block; `mine` is false for threads without partial sums.
+template <int V, int NV, class ColFn>
+__device__ __forceinline__ void add_dgamma(float *dgamma, int H, int G, bool mine, const float (&dg)[NV * V],
+                                           ColFn col_of, float *dgs)
+{
+    const bool v4 = (reinterpret_cast<uintptr_t>(dgamma) & 15) == 0;
+    if (G == 1) {
+        if (!mine) return;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int col = col_of(k);
+            if constexpr (V >= 4) {
+#pragma unroll
+                for (int i = 0; i < V; i += 4)
+                    if (col + i < H) {
+                        if (v4)
+                            red_add_v4(dgamma + col + i, dg[k * V + i], dg[k * V + i + 1], dg[k * V + i + 2],
+                                       dg[k * V + i + 3]);
+                        else
+                            for (int q = 0; q < 4; ++q) atomicAdd(dgamma + col + i + q, dg[k * V + i + q]);
+                    }
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i)
+                    if (col + i < H) atomicAdd(dgamma + col + i, dg[k * V + i]);
+            }
+        }
+        return;
+    }
+    for (int j = threadIdx.x; j < H; j += blockDim.x) dgs[j] = 0.0f;
+    __syncthreads();
+    if (mine) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int col = col_of(k);
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (col + i < H) atomicAdd(dgs + col + i, dg[k * V + i]);
+        }
+    }
+    __syncthreads();
+    for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
+        if (v4 && j + 4 <= H)
+            red_add_v4(dgamma + j, dgs[j], dgs[j + 1], dgs[j + 2], dgs[j + 3]);
+        else
+            for (int q = 0; q < 4 && j + q < H; ++q) atomicAdd(dgamma + j + q, dgs[j + q]);
+    }
+}
+
 // ds = rstd * gamma * dy - (rstd^3 / H) * s * sum(gamma * dy * s) (+ dh), written
-// to dx (and dres); dgamma accumulates dy * s * rstd.  A persistent grid whose
-// blocks hold `groups` rows at a time, `tpr` threads per row: each thread owns
-// the same columns in every row, so gamma and its dgamma partial sums live in
-// registers across the block's rows.  At the end the groups of a block add
-// their partial sums in shared memory and the block adds them to dgamma with
-// 16-byte reductions, one per 4 columns, so global additions number about
-// blocks x H / 4.  The 16-byte path keeps the row's words in registers between
-// the row sum and the gradient; the element path reads them again (cache hits),
-// which keeps its register count within 1024 threads.  Every element is read
-// and written by one thread, reads first, so dx or dres over dy, h or dh is
-// safe.
-template <class T, int EPT, bool VEC>
+// to dx (and dres); dgamma accumulates dy * s * rstd.
+//
+// Rows whose operands are 16-byte aligned: one persistent block of 512
+// threads per SM, split into `groups` teams of `tpr` threads.  A thread owns
+// NV 16-byte columns (the same columns in every row, so gamma and the dgamma
+// partial sums stay in registers); a team covers a whole row and works on
+// R = 4 / NV rows at a time, so every phase of a row (the loads, the row sum's
+// warp reduction and team barrier, the gradient) is paid once for R rows and
+// has R rows of independent work to overlap.  Element pairs use the f32x2
+// forms.
+//
+// A stage (teams x R rows of dy, h and dh, and the rows' rstd values) reaches
+// a ring of `stages` shared-memory stages through the bulk-copy engine
+// (cp.async.bulk, one copy per row and operand; rstd by 4-byte cp.async), all
+// completing on the stage's `full` mbarrier, so the loads in flight per SM are
+// the ring and not what registers can hold.  No warp is set aside to issue
+// them: each warp counts itself out of a stage when it has read it (a
+// per-stage counter that only grows), and the warp whose count completes the
+// stage refills it with the stage `stages` further on.  Rows are read from
+// shared memory twice: the first pass forms d * s once for the row sum
+// sum(gamma * (d * s)) and the dgamma partial sums, the second writes ds.
+// Teams never wait for one another: a row sum is a warp reduction and, for
+// teams of several warps, one named barrier per R rows (the team's own) after
+// which every warp reduces the team's warp sums itself.  Waiting warps sleep
+// in mbarrier try_wait instead of spinning.
+//
+// Every wait is bounded (about a second).  A warp whose wait runs out makes
+// its whole team stop (the decision is taken at the team's barrier, so it is
+// the same for all its warps); a stage that team no longer counts out is never
+// refilled, so the other teams run out of waits in turn.  The block then waits
+// (bounded) for the last copies issued into each stage, counts one timeout and
+// leaves dgamma untouched.
+constexpr int kRmsBwdThreads = 512;
+
+// Two fp32 lanes per instruction (the f32x2 forms of sm_100 and later); each
+// lane is the same IEEE operation, rounded to nearest, as the scalar one.
+struct F2 {
+    float x, y;
+};
+
+__device__ __forceinline__ F2 mul2(F2 a, F2 b)
+{
+    F2 d;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c)
+{
+    F2 d;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ F2 add2(F2 a, F2 b)
+{
+    F2 d;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Element pair q of a 16-byte access (its four words), and back.
+template <class C>
+__device__ __forceinline__ F2 get_pair(const uint32_t (&w)[4], int q)
+{
+    if constexpr (C::kPerWord == 2) return F2{C::get(w[q], 0), C::get(w[q], 1)};
+    else return F2{C::get(w[2 * q], 0), C::get(w[2 * q + 1], 0)};
+}
+
+template <class C>
+__device__ __forceinline__ void put_pair(uint32_t (&w)[4], int q, F2 v)
+{
+    if constexpr (C::kPerWord == 2) {
+        const float f[2] = {v.x, v.y};
+        w[q] = C::put(f);
+    } else {
+        w[2 * q] = C::put(&v.x);
+        w[2 * q + 1] = C::put(&v.y);
+    }
+}
+
+template <class T, bool DH, int NV>
+__global__ void __launch_bounds__(kRmsBwdThreads, 1)
+    add_rmsnorm_bwd_staged_kernel(const BwdParams p)
+{
+    using C = Codec<T>;
+    constexpr int V = 16 / int(sizeof(T));      // elements per 16-byte access
+    constexpr int QV = V / 2;                   // element pairs per access
+    constexpr int R = 4 / NV;                   // rows per team per stage
+    constexpr int W = 4;
+    constexpr int nin = DH ? 3 : 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int TM = p.groups, tpr = p.tpr, S = p.stages;
+    const int SR = TM * R;                      // rows per stage
+    const int warps = (TM * tpr) >> 5, nwg = tpr >> 5;
+    const uint32_t rb = uint32_t(p.H) * uint32_t(sizeof(T));        // one operand row, bytes
+    const uint32_t stage_bytes = uint32_t(SR * nin) * rb;           // layout [operand][stage row][H]
+    unsigned char *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * stage_bytes);
+    int *last_issued = reinterpret_cast<int *>(full + S);           // [S]
+    int *done = last_issued + S;                                    // [S] warps counted out, ever
+    float *rss = reinterpret_cast<float *>(done + S);               // [S][SR] rstd of the staged rows
+    float *red = rss + S * SR;                                      // [2][SR][nwg] warp sums
+    volatile int *gabort = reinterpret_cast<volatile int *>(red + 2 * SR * nwg);   // [2][TM]
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            last_issued[s] = -1;
+            done[s] = 0;
+        }
+        for (int i = 0; i < 2 * TM; ++i) gabort[i] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // iterations per block fit 32 bits: rows of at least 16 bytes in device memory number below 2^35
+    const int64_t n_stages = (p.rows + SR - 1) / SR;
+    const int iters = n_stages > blockIdx.x ? int((n_stages - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    // a whole warp: the copies of iteration `it` into stage it % S
+    const auto issue = [&](int it) {
+        const int64_t base = (int64_t(blockIdx.x) + int64_t(it) * gridDim.x) * SR;
+        const int n = int(p.rows - base < SR ? p.rows - base : SR);
+        const int s = it % S;
+        const uint32_t bar = smem_u32(&full[s]);
+        const uint32_t dst = smem_u32(ring + size_t(s) * stage_bytes);
+        // the rstd copies join the phase before the arrival that can end it
+        if (lane < n) {
+            for (int r = lane; r < n; r += 32) cp_async4(smem_u32(rss + s * SR + r), p.rstd + base + r);
+            cp_async_arrive(bar);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            last_issued[s] = it;
+            mbar_expect_tx(bar, uint32_t(n * nin) * rb);
+        }
+        __syncwarp();
+        for (int j = lane; j < n * nin; j += 32) {
+            const int op = j / n, r = j - op * n;
+            const char *src = op == 0   ? p.dy + (base + r) * p.sdy
+                              : op == 1 ? p.h + (base + r) * p.sh
+                                        : p.dh + (base + r) * p.sdh;
+            bulk_load(dst + uint32_t(op * SR + r) * rb, src, rb, bar);
+        }
+    };
+    if (warp == 0)
+        for (int it = 0; it < S && it < iters; ++it) issue(it);
+
+    const int t = threadIdx.x / tpr, tg = threadIdx.x - t * tpr;     // team, thread within the team
+    const int wig = tg >> 5;
+    const auto column = [&](int k) { return (tg + k * tpr) * V; };
+    F2 dg[NV * QV];
+#pragma unroll
+    for (int i = 0; i < NV * QV; ++i) dg[i] = F2{0.0f, 0.0f};
+    uint32_t gw[NV][W];
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        if (column(k) < p.H) Access<16>::load(p.gamma + int64_t(column(k)) * sizeof(T), gw[k]);
+
+    bool failed = false;
+    for (int it = 0; it < iters; ++it) {
+        const int s = it % S, par = it & 1;
+        const int64_t row0 = (int64_t(blockIdx.x) + int64_t(it) * gridDim.x) * SR + t * R;
+        const bool landed = __all_sync(0xFFFFFFFFu, mbar_wait_sleep(smem_u32(&full[s]), uint32_t((it / S) & 1)));
+        const unsigned char *st = ring + size_t(s) * stage_bytes + size_t(t * R) * rb;
+        const size_t op_stride = size_t(SR) * rb;
+        float rs[R];
+        F2 dot[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            rs[r] = landed && row0 + r < p.rows ? rss[s * SR + t * R + r] : 0.0f;
+            dot[r] = F2{0.0f, 0.0f};
+        }
+        if (landed) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int col = column(k);
+                if (col < p.H) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (row0 + r < p.rows) {
+                            const unsigned char *q0 = st + size_t(r) * rb + size_t(col) * sizeof(T);
+                            const uint4 d4 = *reinterpret_cast<const uint4 *>(q0);
+                            const uint4 s4 = *reinterpret_cast<const uint4 *>(q0 + op_stride);
+                            const uint32_t wd[W] = {d4.x, d4.y, d4.z, d4.w}, ws[W] = {s4.x, s4.y, s4.z, s4.w};
+                            const F2 rs2{rs[r], rs[r]};
+#pragma unroll
+                            for (int q = 0; q < QV; ++q) {
+                                const F2 ds = mul2(get_pair<C>(wd, q), get_pair<C>(ws, q));
+                                dg[k * QV + q] = fma2(ds, rs2, dg[k * QV + q]);
+                                dot[r] = fma2(get_pair<C>(gw[k], q), ds, dot[r]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        float tot[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) tot[r] = warp_sum(dot[r].x + dot[r].y);
+        bool go = landed;
+        if (nwg > 1) {
+            float *rr = red + (par * SR + t * R) * nwg;
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) rr[r * nwg + wig] = tot[r];
+                if (!landed) gabort[par * TM + t] = 1;
+            }
+            named_barrier(1 + t, tpr);
+            go = gabort[par * TM + t] == 0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) tot[r] = warp_sum(lane < nwg ? rr[r * nwg + lane] : 0.0f);
+        }
+        if (!go) {
+            failed = true;
+            break;
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (row0 + r < p.rows) {
+                const float c = rs[r] * rs[r] * rs[r] * (tot[r] / float(p.H));
+                const F2 nc2{-c, -c}, rs2{rs[r], rs[r]};
+                char *dxr = p.dx + (row0 + r) * p.sdx, *drr = p.dres ? p.dres + (row0 + r) * p.sdr : nullptr;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int col = column(k);
+                    if (col < p.H) {
+                        const unsigned char *q0 = st + size_t(r) * rb + size_t(col) * sizeof(T);
+                        const uint4 d4 = *reinterpret_cast<const uint4 *>(q0);
+                        const uint4 s4 = *reinterpret_cast<const uint4 *>(q0 + op_stride);
+                        const uint32_t wd[W] = {d4.x, d4.y, d4.z, d4.w}, ws[W] = {s4.x, s4.y, s4.z, s4.w};
+                        uint32_t we[W] = {0, 0, 0, 0};
+                        if constexpr (DH) {
+                            const uint4 e4 = *reinterpret_cast<const uint4 *>(q0 + 2 * op_stride);
+                            we[0] = e4.x, we[1] = e4.y, we[2] = e4.z, we[3] = e4.w;
+                        }
+                        uint32_t wo[W];
+#pragma unroll
+                        for (int q = 0; q < QV; ++q) {
+                            // rs * gamma * d - c * s (+ dh)
+                            const F2 tq = mul2(mul2(rs2, get_pair<C>(gw[k], q)), get_pair<C>(wd, q));
+                            F2 f = fma2(nc2, get_pair<C>(ws, q), tq);
+                            if constexpr (DH) f = add2(f, get_pair<C>(we, q));
+                            put_pair<C>(wo, q, f);
+                        }
+                        const int64_t off = int64_t(col) * sizeof(T);
+                        Access<16>::store(dxr + off, wo);
+                        if (drr) Access<16>::store(drr + off, wo);
+                    }
+                }
+            }
+        }
+        // count this warp out of stage s; the warp that completes the count refills it
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();      // this warp's reads of the stage before its count
+            last = (atomicAdd(&done[s], 1) + 1) % warps == 0;
+            if (last) __threadfence_block();   // every other warp's count before the refill
+        }
+        if (__shfl_sync(0xFFFFFFFFu, last, 0) && it + S < iters) issue(it + S);
+    }
+    if (__syncthreads_or(failed)) {
+        if (threadIdx.x == 0) {
+            atomicAdd(&g_rms_timeouts, 1u);
+            // the block may only end once every copy it issued has landed
+            for (int s = 0; s < S; ++s) {
+                const int j = last_issued[s];
+                if (j >= 0 && !mbar_wait_sleep(smem_u32(&full[s]), uint32_t((j / S) & 1))) break;
+            }
+        }
+        return;
+    }
+    if (!p.dgamma) return;
+    float dgf[NV * V];
+#pragma unroll
+    for (int i = 0; i < NV * QV; ++i) dgf[2 * i] = dg[i].x, dgf[2 * i + 1] = dg[i].y;
+    // every copy has landed and been read: the ring is free for the team sums
+    add_dgamma<V, NV>(p.dgamma, p.H, TM, true, dgf, column, reinterpret_cast<float *>(ring));
+}
+
+// Rows that are not 16-byte aligned: the same arithmetic with element
+// accesses, each thread owning EPT columns t + k * tpr, one load of each
+// element per pass (the second pass's loads hit the cache).
+template <class T, int EPT>
 __global__ void __launch_bounds__(1024)
     add_rmsnorm_bwd_kernel(const BwdParams p)
 {
     using C = Codec<T>;
-    constexpr int V = VEC ? 16 / int(sizeof(T)) : 1;
-    constexpr int NV = EPT / V;
-    constexpr int W = 4;
     extern __shared__ float dsm[];      // [2][groups][33] row sums, then H floats of dgamma (groups > 1)
     const int G = p.groups, tpr = p.tpr;
-    float *dgs = dsm + 2 * G * 33;
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int g = threadIdx.x / tpr, tg = threadIdx.x - g * tpr;
     const int lane = threadIdx.x & 31, wig = tg >> 5, nwg = tpr >> 5;
-    const auto column = [&](int k) { return VEC ? (tg + k * tpr) * V : tg + k * tpr; };
-    // gamma: the 16-byte path keeps the stored words, the element path fp32 values
-    float gam[VEC ? 1 : EPT], dg[EPT];
-    uint32_t gw[VEC ? NV : 1][W];
+    const auto column = [&](int k) { return tg + k * tpr; };
+    float gam[EPT], dg[EPT];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int col = column(k);
-#pragma unroll
-        for (int i = 0; i < V; ++i) dg[k * V + i] = 0.0f;
-        if constexpr (VEC) {
-            if (col < p.H) Access<16>::load(p.gamma + int64_t(col) * sizeof(T), gw[k]);
-        } else {
-            gam[k] = col < p.H ? C::load1(p.gamma + int64_t(col) * sizeof(T)) : 0.0f;
-        }
+    for (int k = 0; k < EPT; ++k) {
+        dg[k] = 0.0f;
+        gam[k] = column(k) < p.H ? C::load1(p.gamma + int64_t(column(k)) * sizeof(T)) : 0.0f;
     }
-    if (G > 1 && p.dgamma)
-        for (int j = threadIdx.x; j < p.H; j += blockDim.x) dgs[j] = 0.0f;
 
-    // the row sum of this thread's group: warp sums, then (one barrier) each
-    // thread adds its group's warp sums in order, or for groups of more than 8
-    // warps the group's first warp does and a second barrier shares the result
     int parity = 0;
-    const auto group_sum = [&](float v) {
-        float *r = dsm + (parity * G + g) * 33;
-        v = warp_sum(v);
-        if (lane == 0) r[wig] = v;
-        __syncthreads();
-        if (nwg <= 8) {
-            float t = 0.0f;
-            for (int w = 0; w < nwg; ++w) t += r[w];
-            return t;
-        }
-        if (wig == 0) {
-            float t = lane < nwg ? r[lane] : 0.0f;
-            t = warp_sum(t);
-            if (lane == 0) r[32] = t;
-        }
-        __syncthreads();
-        return r[32];
-    };
-
     for (int64_t base = int64_t(blockIdx.x) * G; base < p.rows; base += int64_t(gridDim.x) * G, parity ^= 1) {
         const int64_t row = base + g;
         const bool on = row < p.rows;
@@ -408,126 +742,69 @@ __global__ void __launch_bounds__(1024)
         const char *dhr = p.dh ? p.dh + row * p.sdh : nullptr;
         char *dxr = p.dx + row * p.sdx, *drr = p.dres ? p.dres + row * p.sdr : nullptr;
         SumSq<EPT> dot;
-        if constexpr (VEC) {
-            uint32_t wd[NV][W], ws[NV][W], we[NV][W];
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int col = column(k);
-                if (on && col < p.H) {
-                    const int64_t off = int64_t(col) * sizeof(T);
-                    Access<16>::load(dyr + off, wd[k]);
-                    Access<16>::load(hr + off, ws[k]);
-                    if (dhr) Access<16>::load(dhr + off, we[k]);
-                }
+        for (int k = 0; k < EPT; ++k) {
+            const int col = column(k);
+            if (on && col < p.H) {
+                const int64_t off = int64_t(col) * sizeof(T);
+                dot.add(k, gam[k], C::load1(dyr + off) * C::load1(hr + off));
             }
+        }
+        const float c = rs * rs * rs * (group_sum(dot.total(), dsm + (parity * G + g) * 33, lane, wig, nwg) /
+                                        float(p.H));
 #pragma unroll
-            for (int k = 0; k < NV; ++k)
-                if (on && column(k) < p.H)
-#pragma unroll
-                    for (int j = 0; j < W; ++j)
-#pragma unroll
-                        for (int e = 0; e < C::kPerWord; ++e) {
-                            const int i = k * V + j * C::kPerWord + e;
-                            dot.add(i, C::get(gw[k][j], e) * C::get(wd[k][j], e), C::get(ws[k][j], e));
-                        }
-            const float c = rs * rs * rs * (group_sum(dot.total()) / float(p.H));
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int col = column(k);
-                if (on && col < p.H) {
-                    uint32_t wo[W];
-#pragma unroll
-                    for (int j = 0; j < W; ++j) {
-                        float f[C::kPerWord];
-#pragma unroll
-                        for (int e = 0; e < C::kPerWord; ++e) {
-                            const int i = k * V + j * C::kPerWord + e;
-                            const float d = C::get(wd[k][j], e), sv = C::get(ws[k][j], e);
-                            f[e] = rs * C::get(gw[k][j], e) * d - c * sv;
-                            if (dhr) f[e] += C::get(we[k][j], e);
-                            dg[i] = fmaf(d * sv, rs, dg[i]);
-                        }
-                        wo[j] = C::put(f);
-                    }
-                    const int64_t off = int64_t(col) * sizeof(T);
-                    Access<16>::store(dxr + off, wo);
-                    if (drr) Access<16>::store(drr + off, wo);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < EPT; ++k) {
-                const int col = column(k);
-                if (on && col < p.H) {
-                    const int64_t off = int64_t(col) * sizeof(T);
-                    dot.add(k, gam[k] * C::load1(dyr + off), C::load1(hr + off));
-                }
-            }
-            const float c = rs * rs * rs * (group_sum(dot.total()) / float(p.H));
-#pragma unroll
-            for (int k = 0; k < EPT; ++k) {
-                const int col = column(k);
-                if (on && col < p.H) {
-                    const int64_t off = int64_t(col) * sizeof(T);
-                    const float d = C::load1(dyr + off), sv = C::load1(hr + off);
-                    float v = rs * gam[k] * d - c * sv;
-                    if (dhr) v += C::load1(dhr + off);
-                    dg[k] = fmaf(d * sv, rs, dg[k]);
-                    C::store1(dxr + off, v);
-                    if (drr) C::store1(drr + off, v);
-                }
+        for (int k = 0; k < EPT; ++k) {
+            const int col = column(k);
+            if (on && col < p.H) {
+                const int64_t off = int64_t(col) * sizeof(T);
+                const float d = C::load1(dyr + off), sv = C::load1(hr + off);
+                float v = rs * gam[k] * d - c * sv;
+                if (dhr) v += C::load1(dhr + off);
+                dg[k] = fmaf(d * sv, rs, dg[k]);
+                C::store1(dxr + off, v);
+                if (drr) C::store1(drr + off, v);
             }
         }
     }
     if (!p.dgamma) return;
-    const bool v4 = (reinterpret_cast<uintptr_t>(p.dgamma) & 15) == 0;
-    if (G == 1) {
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int col = column(k);
-            if constexpr (VEC) {
-                // V consecutive columns: 16-byte reductions when dgamma allows
-#pragma unroll
-                for (int i = 0; i < V; i += 4)
-                    if (col + i < p.H) {
-                        if (v4)
-                            red_add_v4(p.dgamma + col + i, dg[k * V + i], dg[k * V + i + 1], dg[k * V + i + 2],
-                                       dg[k * V + i + 3]);
-                        else
-                            for (int q = 0; q < 4; ++q) atomicAdd(p.dgamma + col + i + q, dg[k * V + i + q]);
-                    }
-            } else {
-                if (col < p.H) atomicAdd(p.dgamma + col, dg[k]);
-            }
-        }
-        return;
-    }
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int col = column(k);
-#pragma unroll
-        for (int i = 0; i < V; ++i)
-            if (col + i < p.H) atomicAdd(dgs + col + i, dg[k * V + i]);
-    }
-    __syncthreads();
-    for (int j = threadIdx.x * 4; j < p.H; j += blockDim.x * 4) {
-        if (v4 && j + 4 <= p.H)
-            red_add_v4(p.dgamma + j, dgs[j], dgs[j + 1], dgs[j + 2], dgs[j + 3]);
-        else
-            for (int q = 0; q < 4 && j + q < p.H; ++q) atomicAdd(p.dgamma + j + q, dgs[j + q]);
-    }
+    add_dgamma<1, EPT>(p.dgamma, p.H, G, true, dg, column, dsm + 2 * G * 33);
 }
 
 using BwdFn = void (*)(BwdParams);
 
-BwdFn pick_bwd(int dtype, bool vec)
+template <class T, bool DH>
+BwdFn pick_staged(int nv)
+{
+    return nv == 1 ? add_rmsnorm_bwd_staged_kernel<T, DH, 1>
+                   : nv == 2 ? add_rmsnorm_bwd_staged_kernel<T, DH, 2> : add_rmsnorm_bwd_staged_kernel<T, DH, 4>;
+}
+
+// nv = 0: the element kernel; 1, 2 or 4: the staged kernel with nv 16-byte
+// accesses per operand per thread
+template <class T>
+BwdFn pick_bwd_t(int nv, bool dh)
+{
+    if (nv == 0) return add_rmsnorm_bwd_kernel<T, 16>;
+    return dh ? pick_staged<T, true>(nv) : pick_staged<T, false>(nv);
+}
+
+BwdFn pick_bwd(int dtype, int nv, bool dh)
 {
     switch (dtype) {
-    case GLU_F32: return vec ? add_rmsnorm_bwd_kernel<float, 8, true> : add_rmsnorm_bwd_kernel<float, 16, false>;
-    case GLU_F16: return vec ? add_rmsnorm_bwd_kernel<__half, 16, true> : add_rmsnorm_bwd_kernel<__half, 16, false>;
-    default:
-        return vec ? add_rmsnorm_bwd_kernel<__nv_bfloat16, 16, true> : add_rmsnorm_bwd_kernel<__nv_bfloat16, 16, false>;
+    case GLU_F32: return pick_bwd_t<float>(nv, dh);
+    case GLU_F16: return pick_bwd_t<__half>(nv, dh);
+    default: return pick_bwd_t<__nv_bfloat16>(nv, dh);
     }
+}
+
+cudaError_t timeouts(unsigned int *count, bool reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(count, g_rms_timeouts, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_rms_timeouts, &zero, sizeof(unsigned int));
+    }
+    return e;
 }
 
 using KernelFn = void (*)(Params);
@@ -664,31 +941,73 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     if (n_rows == 1) dy_stride = h_stride = dh_stride = dx_stride = dres_stride = n_cols;
     const auto a16 = [](const void *q) { return uintptr_t(q) % 16 == 0; };
     const auto s16 = [E](int64_t st_) { return (st_ * E) % 16 == 0; };
-    const int vec_ept = 32 / E;      // 16 elements of 16-bit types, 8 of f32: two 16-byte accesses
+    const int V = 16 / E;            // elements per 16-byte access
     const bool vec = a16(dy) && a16(h) && a16(gamma) && a16(dx) && (!dh || a16(dh)) && (!dres || a16(dres)) &&
                      (n_cols * E) % 16 == 0 && s16(dy_stride) && s16(h_stride) && s16(dx_stride) &&
-                     (!dh || s16(dh_stride)) && (!dres || s16(dres_stride)) && n_cols <= int64_t(1024) * vec_ept;
-    const int ept = vec ? vec_ept : 16;
+                     (!dh || s16(dh_stride)) && (!dres || s16(dres_stride)) && n_cols <= int64_t(2048) * V;
+    // 16-byte rows: NV accesses per operand per thread, the fewest that keep a
+    // row within 512 threads; otherwise 16 elements per thread
+    const int nv = !vec ? 0 : n_cols <= int64_t(512) * V ? 1 : n_cols <= int64_t(1024) * V ? 2 : 4;
+    const int ept = vec ? nv * V : 16;
     int tpr = int((n_cols + ept - 1) / ept);
     tpr = (tpr + 31) / 32 * 32;
-    // narrow rows: several rows per block (up to 512 threads), so that fewer
-    // blocks add to dgamma
+    // several rows per block for narrow rows, so that fewer blocks add to
+    // dgamma: the staged kernel's teams fill 512 threads (at most 8 teams of
+    // several warps, one named barrier each, or 16 single-warp teams), the
+    // element kernel up to 512
     const int groups = tpr >= 512 ? 1 : (512 / tpr < 16 ? 512 / tpr : 16);
     const int threads = tpr * groups;
-    const size_t smem = sizeof(float) * (size_t(2 * groups * 33) + (groups > 1 ? size_t(n_cols) : 0));
-    BwdFn fn = pick_bwd(dtype, vec);
+    const int rows_per_stage = vec ? groups * (4 / nv) : groups;
+    BwdFn fn = pick_bwd(dtype, nv, dh != nullptr);
 
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0, sms = 0, smem_sm = 0, smem_block = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void *>(fn), threads, smem);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return glu::cuda_fail(e);
     }
-    const int64_t slots = int64_t(sms) * (per_sm > 0 ? per_sm : 1);
-    const int64_t want = (n_rows + groups - 1) / groups;
+    size_t smem = sizeof(float) * (size_t(2 * groups * 33) + (groups > 1 ? size_t(n_cols) : 0));
+    int stages = 0, per_sm = 1;
+    if (vec) {
+        // One block per SM with the deepest ring of stages (dy, h and dh rows,
+        // the mbarrier, last issued stage, counter and rstd values) that
+        // fits, 8 at most.  A stage holds at most 512 x 64 bytes per operand,
+        // 96 KiB for three, so at least 2 fit.
+        // per device and kernel: the shared-memory limit raised once
+        static std::atomic<int> opted[64][18];
+        std::atomic<int> &flag = opted[dev % 64][((dtype == GLU_F32 ? 0 : dtype == GLU_F16 ? 1 : 2) * 2 +
+                                                   (dh != nullptr)) * 3 + (nv == 4 ? 2 : nv - 1)];
+        if (!flag.load(std::memory_order_acquire)) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem_block);
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                return glu::cuda_fail(e);
+            }
+            flag.store(1, std::memory_order_release);
+        }
+        const size_t stage = size_t(rows_per_stage) * (dh ? 3 : 2) * size_t(n_cols) * E;
+        const size_t per_stage = stage + 8 + 2 * sizeof(int) + size_t(rows_per_stage) * sizeof(float);
+        const size_t fixed =
+            2 * size_t(rows_per_stage) * (tpr / 32) * sizeof(float) + 2 * size_t(groups) * sizeof(int);
+        const int64_t room = int64_t(smem_sm) - 1024 < int64_t(smem_block) ? int64_t(smem_sm) - 1024
+                                                                              : int64_t(smem_block);
+        while (stages < 8 && int64_t((stages + 1) * per_stage + fixed) <= room) ++stages;
+        if (stages < 2) return GLU_ERR_SHAPE;     // not reachable within the column limit
+        smem = size_t(stages) * per_stage + fixed;
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void *>(fn), threads, smem);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return glu::cuda_fail(e);
+        }
+        if (per_sm < 1) per_sm = 1;
+    }
+    const int64_t slots = int64_t(sms) * per_sm;
+    const int64_t want = (n_rows + rows_per_stage - 1) / rows_per_stage;
     const int64_t blocks = want < slots ? want : slots;
 
     BwdParams p{};
@@ -709,6 +1028,7 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     p.H = int(n_cols);
     p.tpr = tpr;
     p.groups = groups;
+    p.stages = stages;
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(blocks));

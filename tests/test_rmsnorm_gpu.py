@@ -230,8 +230,10 @@ def run_bwd(dy, h, rstd, g, dh, dt, dres=False, dgamma=True):
 
 
 TORCH_INT_OF = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}
+# (30011, 64) and (6000, 1024): blocks of 16 and 4 rows that go round the
+# shared-memory ring of the 16-byte path several times, the last group ragged
 BWD_SHAPES = [(1, 1), (3, 7), (5, 64), (77, 100), (33, 1000), (64, 4096), (9, 5000), (17, 8192), (4, 16384),
-              (513, 1536)]
+              (513, 1536), (30011, 64), (6000, 1024)]
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -243,8 +245,14 @@ def test_bwd_parity(orc, shape, dt):
         dx, dg = run_bwd(dy, h, rstd, g, dh, dt, dres=dres)
         info = glu.glu_last_launch()
         E = 4 if dt == "f32" else 2
-        vec = (H * E) % 16 == 0 and H <= 1024 * (32 // E)
+        V = 16 // E
+        vec = (H * E) % 16 == 0 and H <= 2048 * V
         assert info["backward"] == 1 and info["vec_bytes"] == (16 if vec else E) and info["grid"] <= rows
+        # 16-byte rows: the fewest 16-byte accesses per operand per thread (1, 2 or 4) that keep a row
+        # within 512 threads
+        nv = 1 if H <= 512 * V else 2 if H <= 1024 * V else 4
+        assert info["unroll"] == (nv * V if vec else 16)
+        assert glu.glu_wait_timeouts() == 0
         check_bwd(orc, dt, dy, h, rstd, g, dh, dx, dg, f"bwd {dt} {shape} dh={with_dh}")
 
 
