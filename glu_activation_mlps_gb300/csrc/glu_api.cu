@@ -562,6 +562,18 @@ int validate_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_str
 
 namespace glu {
 void record_launch(const glu_launch_info_t &info) { t_last_launch = info; }
+
+cudaError_t on_device(const void *p, bool *yes)
+{
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return e;
+    }
+    *yes = a.type == cudaMemoryTypeDevice;
+    return cudaSuccess;
+}
 }  // namespace glu
 
 extern "C" {
@@ -602,7 +614,7 @@ const char *glu_status_string(int status)
     case GLU_ERR_ENUM: return "unknown activation, layout, dtype or tuning value";
     case GLU_ERR_CUDA: return "the CUDA runtime refused a launch or copy";
     case GLU_ERR_WORKSPACE: return "the workspace is NULL or too small for one row";
-    case GLU_ERR_VALUE: return "an argument is out of range (eps not finite and > 0, or a GEMM operand not in device memory)";
+    case GLU_ERR_VALUE: return "an argument is out of range (eps not finite and > 0, or a GEMM operand or dgamma not in device memory)";
     default: return "unknown status";
     }
 }

@@ -672,20 +672,6 @@ int pick_bn(int64_t m_blocks, int64_t I, int64_t slots)
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_slots[kMaxDevices][2][4][6];
 
-// The tensor-memory accelerator reads and writes device memory only: an
-// operand anywhere else (pinned host memory included) is refused before launch.
-cudaError_t on_device(const void *p, bool *yes)
-{
-    cudaPointerAttributes a{};
-    const cudaError_t e = cudaPointerGetAttributes(&a, p);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return e;
-    }
-    *yes = a.type == cudaMemoryTypeDevice;
-    return cudaSuccess;
-}
-
 bool overlap(uintptr_t a0, uint64_t alen, uintptr_t b0, uint64_t blen)
 {
     return a0 < b0 + blen && b0 < a0 + alen;
@@ -738,9 +724,11 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
         overlap(uintptr_t(y), ylen, uintptr_t(w_up), wlen))
         return GLU_ERR_ALIAS;
 
+    // the tensor-memory accelerator is given device memory only: an operand
+    // anywhere else (pinned host memory included) is refused before launch
     for (const void *q : {x, w_gate, w_up, static_cast<const void *>(y)}) {
         bool dev_mem = false;
-        const cudaError_t pe = on_device(q, &dev_mem);
+        const cudaError_t pe = glu::on_device(q, &dev_mem);
         if (pe != cudaSuccess) return glu::cuda_fail(pe);
         if (!dev_mem) return GLU_ERR_VALUE;
     }

@@ -32,6 +32,10 @@ namespace rms {
 cudaError_t timeouts(unsigned int *count, bool reset);   // glu_rmsnorm.cu
 }
 void record_launch(const glu_launch_info_t &info);       // this thread's glu_last_launch
+// Whether p points into device memory (not pinned host or managed memory):
+// the tensor-memory accelerator and the bulk-copy engine are given device
+// memory only.
+cudaError_t on_device(const void *p, bool *yes);
 
 // Fused residual add + RMSNorm (glu_rmsnorm.cu): argument rules shared with glu_api.cu.
 constexpr int64_t kRmsMaxCols = 32768;

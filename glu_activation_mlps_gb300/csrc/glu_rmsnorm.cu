@@ -937,6 +937,13 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
         glu::record_launch(glu_launch_info_t{});
         return GLU_OK;
     }
+    // dgamma takes atomic reductions: device memory only
+    if (dgamma) {
+        bool dev_mem = false;
+        const cudaError_t pe = glu::on_device(dgamma, &dev_mem);
+        if (pe != cudaSuccess) return glu::cuda_fail(pe);
+        if (!dev_mem) return GLU_ERR_VALUE;
+    }
     const int E = dtype == GLU_F32 ? 4 : 2;
     if (n_rows == 1) dy_stride = h_stride = dh_stride = dx_stride = dres_stride = n_cols;
     const auto a16 = [](const void *q) { return uintptr_t(q) % 16 == 0; };
@@ -945,10 +952,21 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     const bool vec = a16(dy) && a16(h) && a16(gamma) && a16(dx) && (!dh || a16(dh)) && (!dres || a16(dres)) &&
                      (n_cols * E) % 16 == 0 && s16(dy_stride) && s16(h_stride) && s16(dx_stride) &&
                      (!dh || s16(dh_stride)) && (!dres || s16(dres_stride)) && n_cols <= int64_t(2048) * V;
+    // The staged kernel takes 16-byte rows whose inputs are in device memory
+    // (the bulk-copy engine and cp.async are given device memory only);
+    // anything else, pinned host memory included, takes the element kernel.
+    bool staged = vec;
+    for (const void *q : {dy, h, dh, static_cast<const void *>(rstd)}) {
+        if (!staged || !q) continue;
+        bool dev_mem = false;
+        const cudaError_t pe = glu::on_device(q, &dev_mem);
+        if (pe != cudaSuccess) return glu::cuda_fail(pe);
+        staged = dev_mem;
+    }
     // 16-byte rows: NV accesses per operand per thread, the fewest that keep a
     // row within 512 threads; otherwise 16 elements per thread
-    const int nv = !vec ? 0 : n_cols <= int64_t(512) * V ? 1 : n_cols <= int64_t(1024) * V ? 2 : 4;
-    const int ept = vec ? nv * V : 16;
+    const int nv = !staged ? 0 : n_cols <= int64_t(512) * V ? 1 : n_cols <= int64_t(1024) * V ? 2 : 4;
+    const int ept = staged ? nv * V : 16;
     int tpr = int((n_cols + ept - 1) / ept);
     tpr = (tpr + 31) / 32 * 32;
     // several rows per block for narrow rows, so that fewer blocks add to
@@ -957,7 +975,7 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     // element kernel up to 512
     const int groups = tpr >= 512 ? 1 : (512 / tpr < 16 ? 512 / tpr : 16);
     const int threads = tpr * groups;
-    const int rows_per_stage = vec ? groups * (4 / nv) : groups;
+    const int rows_per_stage = staged ? groups * (4 / nv) : groups;
     BwdFn fn = pick_bwd(dtype, nv, dh != nullptr);
 
     int dev = 0, sms = 0, smem_sm = 0, smem_block = 0;
@@ -971,7 +989,7 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     }
     size_t smem = sizeof(float) * (size_t(2 * groups * 33) + (groups > 1 ? size_t(n_cols) : 0));
     int stages = 0, per_sm = 1;
-    if (vec) {
+    if (staged) {
         // One block per SM with the deepest ring of stages (dy, h and dh rows,
         // the mbarrier, last issued stage, counter and rstd values) that
         // fits, 8 at most.  A stage holds at most 512 x 64 bytes per operand,
@@ -1055,7 +1073,7 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     glu_launch_info_t info{};
     info.launched = 1;
     info.backward = 1;
-    info.vec_bytes = vec ? 16 : E;
+    info.vec_bytes = staged ? 16 : E;
     info.unroll = ept;
     info.threads = threads;
     info.grid = int32_t(blocks);

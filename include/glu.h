@@ -25,7 +25,8 @@
  *     stream) and the call returns before it runs.  Pinned host memory
  *     (cudaHostAlloc, cudaHostRegister) is device memory in this sense: the
  *     kernels then read and write it in place over the host link (zero-copy),
- *     except glu_gemm_fwd, whose operands must be in device memory.
+ *     except glu_gemm_fwd's operands and glu_add_rmsnorm_bwd's dgamma, which
+ *     must be in device memory.
  *   - Matrices are row-major with a contiguous last dimension: element (r, c)
  *     of operand X is at X + r * X_stride + c.  Strides are in ELEMENTS of
  *     `dtype`, not bytes, and are ignored when n_rows == 1.
@@ -101,7 +102,8 @@ typedef enum {
     GLU_ERR_CUDA = -6,    /* the CUDA runtime refused a launch or copy; see glu_last_cuda_error() */
     GLU_ERR_WORKSPACE = -7, /* host-memory entry points: workspace NULL or too small for one row */
     GLU_ERR_VALUE = -8      /* an argument out of range: glu_add_rmsnorm_fwd's eps, or an
-                               operand of glu_gemm_fwd that is not in device memory */
+                               operand of glu_gemm_fwd or glu_add_rmsnorm_bwd's dgamma
+                               that is not in device memory */
 } glu_status_t;
 
 /*
@@ -292,8 +294,9 @@ int glu_set_tuning(const glu_tuning_t *t);   /* GLU_ERR_ENUM for unsupported val
 int glu_get_tuning(glu_tuning_t *out);
 
 /* Kernels that wait on the bulk-copy engine or the tensor cores (the bulk-copy
- * path and glu_gemm_fwd) bound every wait (about a second) and count the waits
- * that ran out on the current device instead of hanging.
+ * path, glu_gemm_fwd and glu_add_rmsnorm_bwd's staged kernel) bound every wait
+ * (about a second) and count the waits that ran out on the current device
+ * instead of hanging.
  * Copies that count into *count (synchronising with the device) and, if
  * `reset`, sets it back to 0.  A nonzero count means some outputs of those
  * launches were not written. */
@@ -404,10 +407,19 @@ int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride,
  *                        inputs that dx is not.  dx and dres must not overlap.
  *   dgamma               NULL, or n_cols floats that the row sums are ADDED to
  *                        (zero it for a fresh gradient).  The additions from
- *                        different blocks arrive in no fixed order.
+ *                        different blocks arrive in no fixed order.  It must
+ *                        be in device memory (it takes atomic reductions),
+ *                        else GLU_ERR_VALUE.
  *   n_cols               at most 16384, else GLU_ERR_SHAPE.
  * Other rules as glu_add_rmsnorm_fwd (device pointers, element strides,
  * GLU_ERR_ALIAS for any other overlap, asynchronous on `stream`).
+ *
+ * Rows whose operands are 16-byte aligned (bases, strides, width) and whose
+ * inputs dy, h, dh and rstd are in device memory are staged in shared memory
+ * by the bulk-copy engine; every wait there is bounded (about a second) and
+ * one that runs out is counted by glu_wait_timeouts() and leaves that launch's
+ * outputs and dgamma incomplete.  Other rows (pinned host inputs included)
+ * use element accesses.
  */
 int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride,
                         const void *h, int64_t h_stride,

@@ -289,3 +289,43 @@ def test_forward_then_backward_decoder_block(orc):
     torch.cuda.synchronize()
     check_bwd(orc, "bf16", dy, to_bits(h, "bf16"), rstd.cpu().numpy(), d["gamma"], None, to_bits(dx, "bf16"),
               dg.cpu().numpy(), "decoder block backward")
+
+
+@pytest.mark.parametrize("dt", ("bf16", "f32"))
+def test_pinned_host_memory(orc, dt):
+    """Both entry points on pinned host buffers, through the C calls (the
+    kernels read and write them in place over the host link): the forward on
+    its 16-byte path, the backward on element accesses (its staged kernel takes
+    device-memory inputs only).  dgamma must be in device memory: pinned host
+    memory there is refused before any launch."""
+    rows, H = 300, 1024
+    code, T = {"bf16": (2, torch.bfloat16), "f32": (0, torch.float32)}[dt]
+    pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(
+        {"bf16": np.int16, "f32": np.int32}[dt])).view(T).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    E = 4 if dt == "f32" else 2
+
+    x, r, g = inputs(rows, H, dt, 31)
+    X, RES, GAM = pin(x), pin(r), pin(g)
+    Hh, Y = (torch.empty(rows, H, dtype=T).pin_memory() for _ in range(2))
+    RSTD = torch.empty(rows, dtype=torch.float32).pin_memory()
+    assert glu.glu_add_rmsnorm_fwd(X.data_ptr(), H, RES.data_ptr(), H, GAM.data_ptr(), Hh.data_ptr(), H,
+                                   Y.data_ptr(), H, RSTD.data_ptr(), rows, H, 1e-5, code, s) == 0
+    torch.cuda.synchronize()
+    assert glu.glu_last_launch()["vec_bytes"] == 16
+    check(orc, dt, x, r, g, 1e-5, to_bits(Hh, dt), to_bits(Y, dt), RSTD.numpy(), "pinned forward")
+
+    dy, h, rstd, g2, dh = bwd_inputs(rows, H, dt, 32, True)
+    DY, HH, G2, DH = pin(dy), pin(h), pin(g2), pin(dh)
+    RS = torch.from_numpy(rstd).pin_memory()
+    DX = torch.empty(rows, H, dtype=T).pin_memory()
+    dg = torch.zeros(H, dtype=torch.float32, device="cuda")
+    assert glu.glu_add_rmsnorm_bwd(DY.data_ptr(), H, HH.data_ptr(), H, RS.data_ptr(), G2.data_ptr(), DH.data_ptr(),
+                                   H, DX.data_ptr(), H, None, 0, dg.data_ptr(), rows, H, code, s) == 0
+    torch.cuda.synchronize()
+    assert glu.glu_last_launch()["vec_bytes"] == E
+    check_bwd(orc, dt, dy, h, rstd, g2, dh, to_bits(DX, dt), dg.cpu().numpy(), "pinned backward")
+
+    DG = torch.zeros(H, dtype=torch.float32).pin_memory()
+    assert glu.glu_add_rmsnorm_bwd(DY.data_ptr(), H, HH.data_ptr(), H, RS.data_ptr(), G2.data_ptr(), None, 0,
+                                   DX.data_ptr(), H, None, 0, DG.data_ptr(), rows, H, code, s) == -8   # GLU_ERR_VALUE
