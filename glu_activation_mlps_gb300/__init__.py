@@ -32,7 +32,7 @@ STATUS = {0: "GLU_OK", -1: "GLU_ERR_NULL", -2: "GLU_ERR_SHAPE", -3: "GLU_ERR_STR
 EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_fwd_host_noalloc",
            "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
-           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_gemm_fwd",
+           "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_wait_selftest", "glu_gemm_fwd",
            "glu_add_rmsnorm_fwd", "glu_add_rmsnorm_bwd")
 
 
@@ -107,6 +107,8 @@ def lib() -> ctypes.CDLL:
             L.glu_get_tuning.restype = ci
             L.glu_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
             L.glu_wait_timeouts.restype = ci
+            L.glu_wait_selftest.argtypes = [vp]
+            L.glu_wait_selftest.restype = ci
             L.glu_gemm_fwd.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, i64, ci, ci, vp]
             L.glu_gemm_fwd.restype = ci
             L.glu_add_rmsnorm_fwd.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i64, vp, i64, i64,
@@ -191,6 +193,14 @@ def glu_wait_timeouts(reset: bool = False) -> int:
     if st:
         raise GluError(st, "glu_wait_timeouts")
     return c.value
+
+
+def glu_wait_selftest(stream=None) -> None:
+    """Enqueue the bounded-wait self-test (one warp whose wait nothing
+    completes; it returns after about a second and counts one timeout)."""
+    st = lib().glu_wait_selftest(_stream(stream))
+    if st:
+        raise GluError(st, "glu_wait_selftest")
 
 
 def glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream) -> int:

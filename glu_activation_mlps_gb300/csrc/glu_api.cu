@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "glu.h"
+#include "glu_async.cuh"
 #include "glu_internal.h"
 
 namespace {
@@ -563,6 +564,24 @@ int validate_bwd(const void *dc, int64_t dc_stride, const void *a, int64_t a_str
 namespace glu {
 void record_launch(const glu_launch_info_t &info) { t_last_launch = info; }
 
+// Waits of the self-test kernel that ran out (each launch should add one).
+static __device__ unsigned int g_selftest_timeouts;
+
+// One warp waits on a shared-memory barrier that nothing arrives on, with the
+// bounded, sleeping wait the staged kernels use: the wait must run out and
+// the kernel return.
+__global__ void wait_selftest_kernel()
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const bool completed = __any_sync(0xFFFFFFFFu, mbar_wait_sleep(smem_u32(&bar), 0));
+    if (threadIdx.x == 0 && !completed) atomicAdd(&g_selftest_timeouts, 1u);
+}
+
 cudaError_t on_device(const void *p, bool *yes)
 {
     cudaPointerAttributes a{};
@@ -626,12 +645,30 @@ int glu_version(void) { return GLU_VERSION; }
 int glu_wait_timeouts(unsigned int *count, int reset)
 {
     if (!count) return GLU_ERR_NULL;
-    unsigned int bulk = 0, gemm = 0, rms = 0;
+    unsigned int bulk = 0, gemm = 0, rms = 0, self = 0;
     cudaError_t e = glu::bulk_timeouts(&bulk, reset != 0);
     if (e == cudaSuccess) e = glu::gemm::timeouts(&gemm, reset != 0);
     if (e == cudaSuccess) e = glu::rms::timeouts(&rms, reset != 0);
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&self, glu::g_selftest_timeouts, sizeof(unsigned int));
+    if (e == cudaSuccess && reset) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(glu::g_selftest_timeouts, &zero, sizeof(unsigned int));
+    }
     if (e != cudaSuccess) return cuda_fail(e);
-    *count = bulk + gemm + rms;
+    *count = bulk + gemm + rms + self;
+    return GLU_OK;
+}
+
+int glu_wait_selftest(glu_stream_t stream)
+{
+    glu::wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    glu_launch_info_t info{};
+    info.launched = 1;
+    info.threads = 32;
+    info.grid = 1;
+    glu::record_launch(info);
     return GLU_OK;
 }
 

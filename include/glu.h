@@ -302,6 +302,13 @@ int glu_get_tuning(glu_tuning_t *out);
  * launches were not written. */
 int glu_wait_timeouts(unsigned int *count, int reset);
 
+/* Self-test of that bound: enqueues on `stream` one warp that waits on a
+ * shared-memory barrier nothing arrives on, with the same bounded wait.  The
+ * wait runs out after about a second, the kernel returns, and the count of
+ * glu_wait_timeouts() goes up by one; the context stays usable.  Returns
+ * GLU_OK, or GLU_ERR_CUDA if the launch is refused. */
+int glu_wait_selftest(glu_stream_t stream);
+
 /*
  * Gate and up projections with the gated activation applied in the GEMM
  * epilogue, on the tensor cores:
