@@ -113,6 +113,48 @@ def reduce_max(x: float, device=None) -> float:
     return float(t.item())
 
 
+def link_ceiling(src_host, dst_host, dev_buf, s_a, s_b, reps=5):
+    """GB/s of cudaMemcpyAsync between pinned host memory and the device:
+    host->device, device->host, and both at once on two streams (the bytes of
+    both directions over the time of the pair)."""
+    import torch
+    nbytes = min(src_host.numel() * src_host.element_size(), dst_host.numel() * dst_host.element_size(),
+                 dev_buf.numel() * dev_buf.element_size() // 2)
+    hs = src_host.view(-1).view(torch.uint8)[:nbytes]
+    hd = dst_host.view(-1).view(torch.uint8)[:nbytes]
+    d0, d1 = dev_buf.view(torch.uint8)[:nbytes], dev_buf.view(torch.uint8)[nbytes:2 * nbytes]
+    cur = torch.cuda.current_stream()
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for _ in range(reps):
+            fn()
+        b.record(cur)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def both():
+        s_a.wait_stream(cur)
+        s_b.wait_stream(cur)
+        with torch.cuda.stream(s_a):
+            d0.copy_(hs, non_blocking=True)
+        with torch.cuda.stream(s_b):
+            hd.copy_(d1, non_blocking=True)
+        cur.wait_stream(s_a)
+        cur.wait_stream(s_b)
+
+    h2d = timed(lambda: d0.copy_(hs, non_blocking=True))
+    d2h = timed(lambda: hd.copy_(d1, non_blocking=True))
+    bi = timed(both)
+    return {"h2d_gbs": round(nbytes / h2d / 1e6, 1), "d2h_gbs": round(nbytes / d2h / 1e6, 1),
+            "both_gbs": round(2 * nbytes / bi / 1e6, 1), "bytes": nbytes,
+            "method": "cudaMemcpyAsync by the copy engines on the same pinned buffers; both directions at "
+                      "once on two streams"}
+
+
 def job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> float:
     """Whole-job throughput: every rank runs its own batch (weak scaling), so
     the job moves world * steps * bytes_per_step in the slowest rank's time."""
@@ -344,6 +386,11 @@ def run_gpu(args, rank, world, local_rank):
     zc_ms = reduce_max(e0.elapsed_time(e1), dev)
     barrier()
 
+    # the host link's own ceiling for the e2e number: the copy engines moving
+    # the same pinned bytes one way, the other way, and both ways at once
+    link = link_ceiling(host["a"], out_host["y"], ws, s_in, s_out)
+    barrier()
+
     if rank != 0:
         return None
 
@@ -372,7 +419,9 @@ def run_gpu(args, rank, world, local_rank):
                 "h2d_bytes_per_step": 5 * E * N_ELEMS, "d2h_bytes_per_step": 3 * E * N_ELEMS,
                 "steps": Ke, "ms_per_step": round(zc_ms / Ke, 4),
                 "api": "glu_fwd + glu_bwd on pinned host buffers: the kernels read and write host memory "
-                       "in place over the host link (zero-copy)"},
+                       "in place over the host link (zero-copy)",
+                "link": link,
+                "frac_of_link": round(job_gbs(world, Ke, STEP_BYTES, zc_ms) / world / link["both_gbs"], 4)},
         "e2e_staged": {"value": round(job_gbs(world, Ke, STEP_BYTES, e2e_ms), 1), "unit": UNIT,
                        "h2d_bytes_per_step": 5 * E * N_ELEMS, "d2h_bytes_per_step": 3 * E * N_ELEMS,
                        "steps": Ke, "ms_per_step": round(e2e_ms / Ke, 4),
