@@ -178,8 +178,8 @@ cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, vo
 
 int plan_direct(const Call &c, cudaStream_t stream);
 
-// Bulk-copy staging path: contiguous operands, 16-byte aligned, at least one
-// whole chunk.  Whole chunks go to the bulk kernel (one block per SM), the
+// Bulk-copy staging path: contiguous operands, 16-byte aligned, inputs in
+// device memory, at least one whole chunk.  Whole chunks go to the bulk kernel (one block per SM), the
 // remainder to the direct kernel.  Returns 1 if the call is not eligible.
 int plan_bulk(const Call &c, cudaStream_t stream)
 {
@@ -195,6 +195,16 @@ int plan_bulk(const Call &c, cudaStream_t stream)
     const int64_t bytes = c.rows * c.cols * c.E;
     const int64_t chunks = bytes / glu::kBulkChunkHost;
     if (!flat || chunks < 1) return 1;
+    // the bulk-copy engine is given device memory only: inputs anywhere else
+    // (pinned host memory included) take the direct path
+    const void *inputs[3] = {c.a, c.b, c.dir == kBwd ? c.dc : nullptr};
+    for (const void *q : inputs) {
+        if (!q) continue;
+        bool dev_mem = false;
+        const cudaError_t pe = glu::on_device(q, &dev_mem);
+        if (pe != cudaSuccess) return glu::cuda_fail(pe);
+        if (!dev_mem) return 1;
+    }
 
     // ctas_per_sm 1 selects the wide shape, anything else the narrow one
     const bool narrow = g_ctas_per_sm.load(std::memory_order_relaxed) != 1;

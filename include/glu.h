@@ -279,9 +279,10 @@ int glu_last_launch(glu_launch_info_t *out);
  *                 finish before touching memory, so results and ordering are
  *                 unchanged; only scheduling overlaps); -1: ordinary launch
  *   path          0 or 1: direct 16/32-byte loads into registers; 2: for
- *                 contiguous, 16-byte aligned operands, whole 16 KiB chunks are
- *                 staged in shared memory by the bulk-copy engine (one block
- *                 per SM) and the rest takes the direct path */
+ *                 contiguous, 16-byte aligned operands whose inputs are in
+ *                 device memory, whole 16 KiB chunks are staged in shared
+ *                 memory by the bulk-copy engine (one block per SM) and the
+ *                 rest takes the direct path; everything else takes it too */
 typedef struct {
     int32_t vec_bytes;
     int32_t unroll;

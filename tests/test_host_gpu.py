@@ -150,3 +150,34 @@ def test_device_entry_points_on_pinned_host_memory(orc, dt):
     scale = orc.bwd_da_scale("silu", dt, dc, a, b) if dt == "f32" else None
     helpers.compare(bits(DA), da, dt, scale=scale, what="zero-copy da")
     helpers.compare(bits(DB), db, dt, what="zero-copy db")
+
+
+def test_bulk_path_leaves_pinned_host_inputs_to_direct_loads(orc):
+    """With the bulk-copy path selected, inputs in pinned host memory still take
+    the direct kernels (the bulk-copy engine is given device memory only), and
+    the results are the oracle's."""
+    rows, cols, dt = 300, 2000, "bf16"
+    rng = np.random.default_rng(78)
+    a = glu_synth.normal_bits(rng, (rows, cols), 2.0, dt)
+    b = glu_synth.normal_bits(rng, (rows, cols), 1.0, dt)
+    T = helpers.TORCH[dt]
+    pin = lambda bits: torch.from_numpy(bits.view(helpers.NP_SIGNED[dt])).view(T).pin_memory()
+    A, B = pin(a), pin(b)
+    Y = torch.empty(rows, cols, dtype=T).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    glu.glu_set_tuning(0, 0, 0, 0, 2)
+    try:
+        assert glu.glu_fwd(A.data_ptr(), cols, B.data_ptr(), cols, Y.data_ptr(), cols, rows, cols, 0, 0, 2, s) == 0
+        torch.cuda.synchronize()
+        assert glu.glu_last_launch()["path"] == 1
+        # the same call on device copies does take the bulk path
+        Ad, Bd, Yd = A.cuda(), B.cuda(), torch.empty(rows, cols, dtype=T, device="cuda")
+        assert glu.glu_fwd(Ad.data_ptr(), cols, Bd.data_ptr(), cols, Yd.data_ptr(), cols, rows, cols, 0, 0, 2, s) == 0
+        torch.cuda.synchronize()
+        assert glu.glu_last_launch()["path"] == 2
+    finally:
+        glu.glu_set_tuning(0, 0, 0, 0, 0)
+    bits = lambda t: t.view(helpers.TORCH_INT[dt]).cpu().numpy().view(helpers.NP_BITS[dt])
+    y = orc.fwd("silu", dt, a, b)
+    helpers.compare(bits(Y), y, dt, what="pinned inputs, bulk path selected")
+    helpers.compare(bits(Yd), y, dt, what="device inputs, bulk path")
