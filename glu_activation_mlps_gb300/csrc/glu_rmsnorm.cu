@@ -364,14 +364,13 @@ __device__ __forceinline__ float group_sum(float v, float *r, int lane, int wig,
 // dgamma is 16-byte aligned; with several rows per block the groups first add
 // theirs in the shared array dgs (H floats), then the block adds dgs once, so
 // global additions number about blocks x H / 4.  Called by every thread of
-// the block; `mine` is false for threads without partial sums.
+// the block.
 template <int V, int NV, class ColFn>
-__device__ __forceinline__ void add_dgamma(float *dgamma, int H, int G, bool mine, const float (&dg)[NV * V],
-                                           ColFn col_of, float *dgs)
+__device__ __forceinline__ void add_dgamma(float *dgamma, int H, int G, const float (&dg)[NV * V], ColFn col_of,
+                                           float *dgs)
 {
     const bool v4 = (reinterpret_cast<uintptr_t>(dgamma) & 15) == 0;
     if (G == 1) {
-        if (!mine) return;
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int col = col_of(k);
@@ -395,14 +394,12 @@ __device__ __forceinline__ void add_dgamma(float *dgamma, int H, int G, bool min
     }
     for (int j = threadIdx.x; j < H; j += blockDim.x) dgs[j] = 0.0f;
     __syncthreads();
-    if (mine) {
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int col = col_of(k);
+    for (int k = 0; k < NV; ++k) {
+        const int col = col_of(k);
 #pragma unroll
-            for (int i = 0; i < V; ++i)
-                if (col + i < H) atomicAdd(dgs + col + i, dg[k * V + i]);
-        }
+        for (int i = 0; i < V; ++i)
+            if (col + i < H) atomicAdd(dgs + col + i, dg[k * V + i]);
     }
     __syncthreads();
     for (int j = threadIdx.x * 4; j < H; j += blockDim.x * 4) {
@@ -706,7 +703,7 @@ __global__ void __launch_bounds__(kRmsBwdThreads, 1)
 #pragma unroll
     for (int i = 0; i < NV * QV; ++i) dgf[2 * i] = dg[i].x, dgf[2 * i + 1] = dg[i].y;
     // every copy has landed and been read: the ring is free for the team sums
-    add_dgamma<V, NV>(p.dgamma, p.H, TM, true, dgf, column, reinterpret_cast<float *>(ring));
+    add_dgamma<V, NV>(p.dgamma, p.H, TM, dgf, column, reinterpret_cast<float *>(ring));
 }
 
 // Rows that are not 16-byte aligned: the same arithmetic with element
@@ -726,12 +723,12 @@ __global__ void __launch_bounds__(1024)
     const int g = threadIdx.x / tpr, tg = threadIdx.x - g * tpr;
     const int lane = threadIdx.x & 31, wig = tg >> 5, nwg = tpr >> 5;
     const auto column = [&](int k) { return tg + k * tpr; };
-    float gam[EPT], dg[EPT];
+    // gamma is read where it is used (it stays in L1): keeping it in registers
+    // beside the dgamma partial sums would spill at 1024 threads
+    const auto gam = [&](int col) { return C::load1(p.gamma + int64_t(col) * sizeof(T)); };
+    float dg[EPT];
 #pragma unroll
-    for (int k = 0; k < EPT; ++k) {
-        dg[k] = 0.0f;
-        gam[k] = column(k) < p.H ? C::load1(p.gamma + int64_t(column(k)) * sizeof(T)) : 0.0f;
-    }
+    for (int k = 0; k < EPT; ++k) dg[k] = 0.0f;
 
     int parity = 0;
     for (int64_t base = int64_t(blockIdx.x) * G; base < p.rows; base += int64_t(gridDim.x) * G, parity ^= 1) {
@@ -747,7 +744,7 @@ __global__ void __launch_bounds__(1024)
             const int col = column(k);
             if (on && col < p.H) {
                 const int64_t off = int64_t(col) * sizeof(T);
-                dot.add(k, gam[k], C::load1(dyr + off) * C::load1(hr + off));
+                dot.add(k, gam(col), C::load1(dyr + off) * C::load1(hr + off));
             }
         }
         const float c = rs * rs * rs * (group_sum(dot.total(), dsm + (parity * G + g) * 33, lane, wig, nwg) /
@@ -758,7 +755,7 @@ __global__ void __launch_bounds__(1024)
             if (on && col < p.H) {
                 const int64_t off = int64_t(col) * sizeof(T);
                 const float d = C::load1(dyr + off), sv = C::load1(hr + off);
-                float v = rs * gam[k] * d - c * sv;
+                float v = rs * gam(col) * d - c * sv;
                 if (dhr) v += C::load1(dhr + off);
                 dg[k] = fmaf(d * sv, rs, dg[k]);
                 C::store1(dxr + off, v);
@@ -767,7 +764,7 @@ __global__ void __launch_bounds__(1024)
         }
     }
     if (!p.dgamma) return;
-    add_dgamma<1, EPT>(p.dgamma, p.H, G, true, dg, column, dsm + 2 * G * 33);
+    add_dgamma<1, EPT>(p.dgamma, p.H, G, dg, column, dsm + 2 * G * 33);
 }
 
 using BwdFn = void (*)(BwdParams);
