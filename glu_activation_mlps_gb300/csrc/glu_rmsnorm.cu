@@ -321,8 +321,8 @@ struct BwdParams {
     int64_t rows;
     int H;
     int tpr;                            // threads per row (a multiple of 32)
-    int groups;                         // rows a block works on at once
-    int stages;                         // staged kernel: shared-memory ring depth, in row groups
+    int groups;                         // rows a block works on at once (staged kernel: teams)
+    int stages;                         // staged kernel: shared-memory ring depth, in stages
 };
 
 // Waits of the staged backward that ran out, summed since the last reset.
