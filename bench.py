@@ -587,6 +587,59 @@ def run_table(args):
 GM, GK, GI = 4096, 4096, 14336      # tokens, hidden size, intermediate size of one MLP layer
 
 
+# Other layer shapes for --gemm: token counts from decode (1, 64, 128) to a
+# large batch (8192), and a wider layer (hidden 8192, intermediate 28672).
+GEMM_SHAPES = ((8192, 4096, 14336), (2048, 4096, 14336), (1024, 4096, 14336), (4096, 8192, 28672),
+               (128, 8192, 28672), (64, 4096, 14336), (1, 8192, 28672))
+
+
+def tile_columns(M, I, info):
+    """The column-tile width a glu_gemm_fwd launch used, from its tile count."""
+    m_blocks = -(-M // (128 * info["unroll"]))
+    i_blocks = info["vector_units"] // m_blocks
+    return next(bn for bn in (64, 96, 128) if -(-I // bn) == i_blocks)
+
+
+def gemm_shapes(L, glu, timed, dev, s, K, W):
+    """glu_gemm_fwd against cuBLAS alone and cuBLAS then glu_fwd, per shape."""
+    import torch
+    out = []
+    for (M, Kd, I) in GEMM_SHAPES:
+        gen = torch.Generator(device=dev).manual_seed(7)
+        x = torch.randn(M, Kd, device=dev, generator=gen).to(torch.bfloat16)
+        w = (torch.randn(2 * I, Kd, device=dev, generator=gen) / Kd ** 0.5).to(torch.bfloat16)
+        y = torch.empty(M, I, device=dev, dtype=torch.bfloat16)
+        h = torch.empty(M, 2 * I, device=dev, dtype=torch.bfloat16)
+        wg, wu = w[:I], w[I:]
+
+        def fused():
+            st = L.glu_gemm_fwd(x.data_ptr(), Kd, wg.data_ptr(), wu.data_ptr(), Kd, y.data_ptr(), I, M, Kd, I, 0,
+                                2, s)
+            if st:
+                raise glu.GluError(st, "glu_gemm_fwd")
+
+        def unfused():
+            torch.matmul(x, w.T, out=h)
+            st = L.glu_fwd(h.data_ptr(), 2 * I, None, 0, y.data_ptr(), I, M, I, 1, 0, 2, s)
+            if st:
+                raise glu.GluError(st, "glu_fwd")
+
+        f_ms = timed(fused, K, W)
+        info = glu.glu_last_launch()
+        g_ms = timed(lambda: torch.matmul(x, w.T, out=h), K, W)
+        u_ms = timed(unfused, K, W)
+        fl = 2 * M * Kd * 2 * I
+        out.append({"M": M, "K": Kd, "I": I, "fused_ms": round(f_ms, 4),
+                    "fused_tflops": round(fl / (f_ms * 1e-3) / 1e12, 1),
+                    "weights_gbs": round(2 * I * Kd * 2 / (f_ms * 1e-3) / 1e9, 1),
+                    "cublas_gemm_ms": round(g_ms, 4), "cublas_gemm_plus_glu_fwd_ms": round(u_ms, 4),
+                    "vs_cublas_gemm": round(g_ms / f_ms, 3), "vs_unfused": round(u_ms / f_ms, 3),
+                    "tile_columns": tile_columns(M, I, info), "tiles": info["vector_units"],
+                    "cluster": info["unroll"]})
+        del x, w, y, h
+    return out
+
+
 def run_gemm(args):
     """The gate/up projections with SwiGLU in the epilogue (glu_gemm_fwd) on one
     MLP layer, against the unfused path it replaces: one cuBLAS GEMM into a
@@ -648,6 +701,7 @@ def run_gemm(args):
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     peak = float(peaks["bf16_tflops"])
     tf = flops / (fused_ms * 1e-3) / 1e12
+    shapes = gemm_shapes(L, glu, timed, dev, s, max(5, min(K, 50)), W) if not args.no_sweep else []
     line = {
         "metric": "gate/up projections with SwiGLU in the epilogue, TFLOP/s (bf16, M=4096 K=4096 I=14336)",
         "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W,
@@ -664,6 +718,7 @@ def run_gemm(args):
                        "cublas_gemm_tflops": round(flops / (gemm_ms * 1e-3) / 1e12, 1),
                        "cublas_gemm_plus_glu_fwd_ms": round(unfused_ms, 4),
                        "speedup_vs_unfused": round(unfused_ms / fused_ms, 4)},
+        "shapes": shapes,
         "gpu_launches": K,
         "clocks": clock_info,
     }
@@ -876,6 +931,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--gemm", action="store_true",
                     help="time glu_gemm_fwd on one MLP layer against cuBLAS + glu_fwd (one JSON line)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="--gemm: skip the other layer shapes")
     ap.add_argument("--rmsnorm", action="store_true",
                     help="time glu_add_rmsnorm_fwd on one decoder block against torch's add + rms_norm")
     ap.add_argument("--table", action="store_true",

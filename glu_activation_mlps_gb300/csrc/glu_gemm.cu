@@ -646,19 +646,22 @@ Variant pick(bool bf16, int act, int bn, int ctas)
     return bn == 96 ? variant<96, 2>(bf16, act, 4) : variant<128, 2>(bf16, act, 5);
 }
 
-// Column-tile width: every tile of one width costs about the same, so the
-// launch takes ceil(tiles / slots) rounds of tiles BN columns wide; pick the
-// width with the fewest columns in its rounds (the widest on a tie: wider
-// tiles move fewer bytes per FLOP).  With 152 SMs and I = 14336, M <= 128
-// gets 96 (150 tiles, one round) instead of 128 (112 tiles on 152 SMs).
-int pick_bn(int64_t m_blocks, int64_t I, int64_t slots)
+// Column-tile width.  The kernel is bound by the stream of operand tiles into
+// shared memory: a tile BN columns wide moves a_rows rows of x (both blocks
+// of a pair together) and 2 BN rows of weights per K step, and the launch
+// takes ceil(tiles / slots) rounds of such tiles.  Pick the width whose rounds
+// move the fewest rows (the widest on a tie).  Measured on GB300: with 152 SMs
+// and I = 14336, M <= 128 gets 96 (150 tiles in one round, fewer weight rows
+// per block than 128); M = 8192 gets 128 where a rule on columns alone picked
+// 64 for 1 % less wave quantisation and ran 1.8 times slower.
+int pick_bn(int64_t m_blocks, int64_t I, int64_t slots, int64_t a_rows)
 {
     if (I <= 64) return 64;
     int best = 128;
     int64_t best_cost = -1;
     for (int bn : {128, 96, 64}) {
         const int64_t tiles = m_blocks * ((I + bn - 1) / bn);
-        const int64_t cost = (tiles + slots - 1) / slots * bn;
+        const int64_t cost = (tiles + slots - 1) / slots * (a_rows + 2 * bn);
         if (best_cost < 0 || cost < best_cost) {
             best = bn;
             best_cost = cost;
@@ -739,7 +742,8 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
     const int64_t rows_per_block = int64_t(BM) * ctas;
-    const int bn = pick_bn((M + rows_per_block - 1) / rows_per_block, I, sms / ctas);
+    const int64_t tile_rows = ctas == 1 ? (M + 7) / 8 * 8 : rows_per_block;     // rows of x a tile loads
+    const int bn = pick_bn((M + rows_per_block - 1) / rows_per_block, I, sms / ctas, tile_rows);
     const Variant v = pick(bf16, act, bn, ctas);
 
     cudaLaunchConfig_t cfg{};

@@ -90,10 +90,12 @@ def check_bound(orc, act, dt, y_bits, g, u, sg, su, K, what):
 
 # M <= 128 runs one block per tile, larger M pairs of blocks on 256 rows;
 # column tiles are 64, 96 or 128 wide (the rule in expected_tiles), and the
-# shapes below take each width in both block shapes.
+# shapes below take each width in both block shapes: one block 96 at
+# (5, 520, 14336) and 128 at (100, 64, 38912); pairs 96 at (256, 64, 14336)
+# and 128 at (1024, 16, 14336); 64 elsewhere.
 SHAPES = [(1, 8, 1), (128, 64, 128), (127, 72, 65), (300, 200, 300), (129, 1000, 40), (257, 328, 200),
           (64, 4096, 64), (700, 256, 520), (333, 136, 100), (5, 520, 14336), (256, 64, 14336),
-          (100, 64, 38912)]
+          (100, 64, 38912), (1024, 16, 14336)]
 
 
 def cluster_size(M, I):
@@ -102,17 +104,19 @@ def cluster_size(M, I):
 
 def expected_tiles(M, I, sms):
     """The library's tile-width rule: the width in {128, 96, 64} whose rounds of
-    tiles (ceil(tiles / slots) of them) span the fewest columns, the widest on a
-    tie; 64 when I fits one tile."""
+    tiles (ceil(tiles / slots) of them) move the fewest operand rows per K step
+    (a tile's rows of x, 256 for a pair or M rounded up to 8 for one block, plus
+    2 x width rows of weights), the widest on a tie; 64 when I fits one tile."""
     ctas = cluster_size(M, I)
     m_blocks = -(-M // (128 * ctas))
     slots = sms // ctas
+    a_rows = 256 if ctas == 2 else -(-M // 8) * 8
     if I <= 64:
         return m_blocks
     best = None
     for bn in (128, 96, 64):
         tiles = m_blocks * -(-I // bn)
-        cost = -(-tiles // slots) * bn
+        cost = -(-tiles // slots) * (a_rows + 2 * bn)
         if best is None or cost < best[0]:
             best = (cost, tiles)
     return best[1]
