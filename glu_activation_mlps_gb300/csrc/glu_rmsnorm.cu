@@ -413,37 +413,43 @@ __device__ __forceinline__ void add_dgamma(float *dgamma, int H, int G, const fl
 // ds = rstd * gamma * dy - (rstd^3 / H) * s * sum(gamma * dy * s) (+ dh), written
 // to dx (and dres); dgamma accumulates dy * s * rstd.
 //
-// Rows whose operands are 16-byte aligned: one persistent block of 512
-// threads per SM, split into `groups` teams of `tpr` threads.  A thread owns
-// NV 16-byte columns (the same columns in every row, so gamma and the dgamma
-// partial sums stay in registers); a team covers a whole row and works on
-// R = 4 / NV rows at a time, so every phase of a row (the loads, the row sum's
-// warp reduction and team barrier, the gradient) is paid once for R rows and
-// has R rows of independent work to overlap.  Element pairs use the f32x2
-// forms.
+// Rows whose operands are 16-byte aligned and whose inputs are in device
+// memory: one persistent block per SM whose threads form `groups` teams of
+// `tpr` threads.  A thread owns NV 16-byte columns (the same columns in every
+// row, so gamma and the dgamma partial sums stay in registers); a team covers
+// a whole row and works on R rows at a time, so every phase of a row (the
+// loads, the row sum's warp reduction and team barrier, the gradient) is paid
+// once for R rows and has R rows of independent work to overlap.  Element
+// pairs use the f32x2 forms.
 //
 // A stage (teams x R rows of dy, h and dh, and the rows' rstd values) reaches
 // a ring of `stages` shared-memory stages through the bulk-copy engine
 // (cp.async.bulk, one copy per row and operand; rstd by 4-byte cp.async), all
 // completing on the stage's `full` mbarrier, so the loads in flight per SM are
-// the ring and not what registers can hold.  No warp is set aside to issue
-// them: each warp counts itself out of a stage when it has read it (a
-// per-stage counter that only grows), and the warp whose count completes the
-// stage refills it with the stage `stages` further on.  Rows are read from
-// shared memory twice: the first pass forms d * s once for the row sum
-// sum(gamma * (d * s)) and the dgamma partial sums, the second writes ds.
-// Teams never wait for one another: a row sum is a warp reduction and, for
-// teams of several warps, one named barrier per R rows (the team's own) after
-// which every warp reduces the team's warp sums itself.  Waiting warps sleep
-// in mbarrier try_wait instead of spinning.
+// the ring and not what registers can hold.  Issuing a stage's copies holds
+// the issuing warp for about a thousand cycles, so who issues them matters:
+//   - PROD (rows of up to 1024 vectors): a producer warp, the block's last,
+//     issues every stage once all 8 consumer warps have arrived on the stage's
+//     `empty` mbarrier; consumers never issue.  R = 8 / NV rows per team.
+//   - otherwise (wider rows, NV = 4 at 512 threads, whose 16 warps leave no
+//     registers for a producer warp): each warp counts itself out of a stage
+//     when it has read it (a per-stage counter that only grows), and the warp
+//     whose count completes the stage refills it.  R = 4 / NV.
+// Rows are read from shared memory twice: the first pass forms d * s once for
+// the row sum sum(gamma * (d * s)) and the dgamma partial sums, the second
+// writes ds.  Teams never wait for one another: a row sum is a warp reduction
+// and, for teams of several warps, one named barrier per R rows (the team's
+// own) after which every warp reduces the team's warp sums itself.  Waiting
+// warps sleep in mbarrier try_wait instead of spinning.
 //
 // Every wait is bounded (about a second).  A warp whose wait runs out makes
 // its whole team stop (the decision is taken at the team's barrier, so it is
-// the same for all its warps); a stage that team no longer counts out is never
-// refilled, so the other teams run out of waits in turn.  The block then waits
-// (bounded) for the last copies issued into each stage, counts one timeout and
+// the same for all its warps); a stage that team no longer releases is never
+// refilled, so the other teams and the producer run out of waits in turn.  The
+// block then waits (bounded) for the copies it issued, counts one timeout and
 // leaves dgamma untouched.
-constexpr int kRmsBwdThreads = 512;
+constexpr int kRmsBwdConsumersP = 256;      // consumer threads beside the producer warp
+constexpr int kRmsBwdThreads = 512;         // threads of the block without one
 
 // Two fp32 lanes per instruction (the f32x2 forms of sm_100 and later); each
 // lane is the same IEEE operation, rounded to nearest, as the scalar one.
@@ -501,27 +507,29 @@ __device__ __forceinline__ void put_pair(uint32_t (&w)[4], int q, F2 v)
     }
 }
 
-template <class T, bool DH, int NV>
-__global__ void __launch_bounds__(kRmsBwdThreads, 1)
+template <class T, bool DH, int NV, bool PROD>
+__global__ void __launch_bounds__(PROD ? kRmsBwdConsumersP + 32 : kRmsBwdThreads, 1)
     add_rmsnorm_bwd_staged_kernel(const BwdParams p)
 {
     using C = Codec<T>;
     constexpr int V = 16 / int(sizeof(T));      // elements per 16-byte access
     constexpr int QV = V / 2;                   // element pairs per access
-    constexpr int R = 4 / NV;                   // rows per team per stage
+    constexpr int R = (PROD ? 8 : 4) / NV;      // rows per team per stage
     constexpr int W = 4;
     constexpr int nin = DH ? 3 : 2;
     extern __shared__ __align__(128) unsigned char smem[];
     const int TM = p.groups, tpr = p.tpr, S = p.stages;
     const int SR = TM * R;                      // rows per stage
-    const int warps = (TM * tpr) >> 5, nwg = tpr >> 5;
+    const int consumers = TM * tpr;
+    const int warps = consumers >> 5, nwg = tpr >> 5;
     const uint32_t rb = uint32_t(p.H) * uint32_t(sizeof(T));        // one operand row, bytes
     const uint32_t stage_bytes = uint32_t(SR * nin) * rb;           // layout [operand][stage row][H]
     unsigned char *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * stage_bytes);
-    int *last_issued = reinterpret_cast<int *>(full + S);           // [S]
-    int *done = last_issued + S;                                    // [S] warps counted out, ever
-    float *rss = reinterpret_cast<float *>(done + S);               // [S][SR] rstd of the staged rows
+    uint64_t *empty = full + S;                                     // PROD: [S] consumer warps done
+    int *last_issued = reinterpret_cast<int *>(full + S);           // otherwise: [S], then
+    int *done = last_issued + S;                                    //   [S] warps counted out, ever
+    float *rss = reinterpret_cast<float *>(full + 2 * S);           // [S][SR] rstd of the staged rows
     float *red = rss + S * SR;                                      // [2][SR][nwg] warp sums
     volatile int *gabort = reinterpret_cast<volatile int *>(red + 2 * SR * nwg);   // [2][TM]
 
@@ -531,8 +539,12 @@ __global__ void __launch_bounds__(kRmsBwdThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            last_issued[s] = -1;
-            done[s] = 0;
+            if constexpr (PROD) {
+                mbar_init(smem_u32(&empty[s]), uint32_t(warps));
+            } else {
+                last_issued[s] = -1;
+                done[s] = 0;
+            }
         }
         for (int i = 0; i < 2 * TM; ++i) gabort[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(kRmsBwdThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
-            last_issued[s] = it;
+            if constexpr (!PROD) last_issued[s] = it;
             mbar_expect_tx(bar, uint32_t(n * nin) * rb);
         }
         __syncwarp();
@@ -570,130 +582,162 @@ __global__ void __launch_bounds__(kRmsBwdThreads, 1)
             bulk_load(dst + uint32_t(op * SR + r) * rb, src, rb, bar);
         }
     };
-    if (warp == 0)
-        for (int it = 0; it < S && it < iters; ++it) issue(it);
 
     const int t = threadIdx.x / tpr, tg = threadIdx.x - t * tpr;     // team, thread within the team
-    const int wig = tg >> 5;
     const auto column = [&](int k) { return (tg + k * tpr) * V; };
     F2 dg[NV * QV];
 #pragma unroll
     for (int i = 0; i < NV * QV; ++i) dg[i] = F2{0.0f, 0.0f};
-    uint32_t gw[NV][W];
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-        if (column(k) < p.H) Access<16>::load(p.gamma + int64_t(column(k)) * sizeof(T), gw[k]);
-
     bool failed = false;
-    for (int it = 0; it < iters; ++it) {
-        const int s = it % S, par = it & 1;
-        const int64_t row0 = (int64_t(blockIdx.x) + int64_t(it) * gridDim.x) * SR + t * R;
-        const bool landed = __all_sync(0xFFFFFFFFu, mbar_wait_sleep(smem_u32(&full[s]), uint32_t((it / S) & 1)));
-        const unsigned char *st = ring + size_t(s) * stage_bytes + size_t(t * R) * rb;
-        const size_t op_stride = size_t(SR) * rb;
-        float rs[R];
-        F2 dot[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            rs[r] = landed && row0 + r < p.rows ? rss[s * SR + t * R + r] : 0.0f;
-            dot[r] = F2{0.0f, 0.0f};
+
+    if (PROD && threadIdx.x >= consumers) {
+        // the producer warp: stage it % S is filled for the (it / S)-th time
+        int it = 0;
+        for (; it < iters; ++it) {
+            if (it >= S) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_sleep(smem_u32(&empty[it % S]), uint32_t((it / S - 1) & 1));
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                    failed = true;
+                    break;
+                }
+            }
+            issue(it);
         }
-        if (landed) {
+        // the block may only end once every copy it issued has landed
+        bool ok = true;
+        if (lane == 0)
+            for (int j = it > S ? it - S : 0; j < it && ok; ++j)
+                ok = mbar_wait_sleep(smem_u32(&full[j % S]), uint32_t((j / S) & 1));
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) failed = true;
+    } else {
+        if (!PROD && warp == 0)
+            for (int it = 0; it < S && it < iters; ++it) issue(it);
+        const int wig = tg >> 5;
+        uint32_t gw[NV][W];
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int col = column(k);
-                if (col < p.H) {
+        for (int k = 0; k < NV; ++k)
+            if (column(k) < p.H) Access<16>::load(p.gamma + int64_t(column(k)) * sizeof(T), gw[k]);
+
+        for (int it = 0; it < iters; ++it) {
+            const int s = it % S, par = it & 1;
+            const int64_t row0 = (int64_t(blockIdx.x) + int64_t(it) * gridDim.x) * SR + t * R;
+            const bool landed =
+                __all_sync(0xFFFFFFFFu, mbar_wait_sleep(smem_u32(&full[s]), uint32_t((it / S) & 1)));
+            const unsigned char *st = ring + size_t(s) * stage_bytes + size_t(t * R) * rb;
+            const size_t op_stride = size_t(SR) * rb;
+            float rs[R];
+            F2 dot[R];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        if (row0 + r < p.rows) {
-                            const unsigned char *q0 = st + size_t(r) * rb + size_t(col) * sizeof(T);
-                            const uint4 d4 = *reinterpret_cast<const uint4 *>(q0);
-                            const uint4 s4 = *reinterpret_cast<const uint4 *>(q0 + op_stride);
-                            const uint32_t wd[W] = {d4.x, d4.y, d4.z, d4.w}, ws[W] = {s4.x, s4.y, s4.z, s4.w};
-                            const F2 rs2{rs[r], rs[r]};
+            for (int r = 0; r < R; ++r) {
+                rs[r] = landed && row0 + r < p.rows ? rss[s * SR + t * R + r] : 0.0f;
+                dot[r] = F2{0.0f, 0.0f};
+            }
+            if (landed) {
 #pragma unroll
-                            for (int q = 0; q < QV; ++q) {
-                                const F2 ds = mul2(get_pair<C>(wd, q), get_pair<C>(ws, q));
-                                dg[k * QV + q] = fma2(ds, rs2, dg[k * QV + q]);
-                                dot[r] = fma2(get_pair<C>(gw[k], q), ds, dot[r]);
+                for (int k = 0; k < NV; ++k) {
+                    const int col = column(k);
+                    if (col < p.H) {
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            if (row0 + r < p.rows) {
+                                const unsigned char *q0 = st + size_t(r) * rb + size_t(col) * sizeof(T);
+                                const uint4 d4 = *reinterpret_cast<const uint4 *>(q0);
+                                const uint4 s4 = *reinterpret_cast<const uint4 *>(q0 + op_stride);
+                                const uint32_t wd[W] = {d4.x, d4.y, d4.z, d4.w}, ws[W] = {s4.x, s4.y, s4.z, s4.w};
+                                const F2 rs2{rs[r], rs[r]};
+#pragma unroll
+                                for (int q = 0; q < QV; ++q) {
+                                    const F2 ds = mul2(get_pair<C>(wd, q), get_pair<C>(ws, q));
+                                    dg[k * QV + q] = fma2(ds, rs2, dg[k * QV + q]);
+                                    dot[r] = fma2(get_pair<C>(gw[k], q), ds, dot[r]);
+                                }
                             }
                         }
                     }
                 }
             }
-        }
-        float tot[R];
+            float tot[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) tot[r] = warp_sum(dot[r].x + dot[r].y);
-        bool go = landed;
-        if (nwg > 1) {
-            float *rr = red + (par * SR + t * R) * nwg;
-            if (lane == 0) {
+            for (int r = 0; r < R; ++r) tot[r] = warp_sum(dot[r].x + dot[r].y);
+            bool go = landed;
+            if (nwg > 1) {
+                float *rr = red + (par * SR + t * R) * nwg;
+                if (lane == 0) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) rr[r * nwg + wig] = tot[r];
-                if (!landed) gabort[par * TM + t] = 1;
+                    for (int r = 0; r < R; ++r) rr[r * nwg + wig] = tot[r];
+                    if (!landed) gabort[par * TM + t] = 1;
+                }
+                named_barrier(1 + t, tpr);
+                go = gabort[par * TM + t] == 0;
+#pragma unroll
+                for (int r = 0; r < R; ++r) tot[r] = warp_sum(lane < nwg ? rr[r * nwg + lane] : 0.0f);
             }
-            named_barrier(1 + t, tpr);
-            go = gabort[par * TM + t] == 0;
+            if (!go) {
+                failed = true;
+                break;
+            }
 #pragma unroll
-            for (int r = 0; r < R; ++r) tot[r] = warp_sum(lane < nwg ? rr[r * nwg + lane] : 0.0f);
-        }
-        if (!go) {
-            failed = true;
-            break;
-        }
+            for (int r = 0; r < R; ++r) {
+                if (row0 + r < p.rows) {
+                    const float c = rs[r] * rs[r] * rs[r] * (tot[r] / float(p.H));
+                    const F2 nc2{-c, -c}, rs2{rs[r], rs[r]};
+                    char *dxr = p.dx + (row0 + r) * p.sdx, *drr = p.dres ? p.dres + (row0 + r) * p.sdr : nullptr;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (row0 + r < p.rows) {
-                const float c = rs[r] * rs[r] * rs[r] * (tot[r] / float(p.H));
-                const F2 nc2{-c, -c}, rs2{rs[r], rs[r]};
-                char *dxr = p.dx + (row0 + r) * p.sdx, *drr = p.dres ? p.dres + (row0 + r) * p.sdr : nullptr;
+                    for (int k = 0; k < NV; ++k) {
+                        const int col = column(k);
+                        if (col < p.H) {
+                            const unsigned char *q0 = st + size_t(r) * rb + size_t(col) * sizeof(T);
+                            const uint4 d4 = *reinterpret_cast<const uint4 *>(q0);
+                            const uint4 s4 = *reinterpret_cast<const uint4 *>(q0 + op_stride);
+                            const uint32_t wd[W] = {d4.x, d4.y, d4.z, d4.w}, ws[W] = {s4.x, s4.y, s4.z, s4.w};
+                            uint32_t we[W] = {0, 0, 0, 0};
+                            if constexpr (DH) {
+                                const uint4 e4 = *reinterpret_cast<const uint4 *>(q0 + 2 * op_stride);
+                                we[0] = e4.x, we[1] = e4.y, we[2] = e4.z, we[3] = e4.w;
+                            }
+                            uint32_t wo[W];
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int col = column(k);
-                    if (col < p.H) {
-                        const unsigned char *q0 = st + size_t(r) * rb + size_t(col) * sizeof(T);
-                        const uint4 d4 = *reinterpret_cast<const uint4 *>(q0);
-                        const uint4 s4 = *reinterpret_cast<const uint4 *>(q0 + op_stride);
-                        const uint32_t wd[W] = {d4.x, d4.y, d4.z, d4.w}, ws[W] = {s4.x, s4.y, s4.z, s4.w};
-                        uint32_t we[W] = {0, 0, 0, 0};
-                        if constexpr (DH) {
-                            const uint4 e4 = *reinterpret_cast<const uint4 *>(q0 + 2 * op_stride);
-                            we[0] = e4.x, we[1] = e4.y, we[2] = e4.z, we[3] = e4.w;
+                            for (int q = 0; q < QV; ++q) {
+                                // rs * gamma * d - c * s (+ dh)
+                                const F2 tq = mul2(mul2(rs2, get_pair<C>(gw[k], q)), get_pair<C>(wd, q));
+                                F2 f = fma2(nc2, get_pair<C>(ws, q), tq);
+                                if constexpr (DH) f = add2(f, get_pair<C>(we, q));
+                                put_pair<C>(wo, q, f);
+                            }
+                            const int64_t off = int64_t(col) * sizeof(T);
+                            Access<16>::store(dxr + off, wo);
+                            if (drr) Access<16>::store(drr + off, wo);
                         }
-                        uint32_t wo[W];
-#pragma unroll
-                        for (int q = 0; q < QV; ++q) {
-                            // rs * gamma * d - c * s (+ dh)
-                            const F2 tq = mul2(mul2(rs2, get_pair<C>(gw[k], q)), get_pair<C>(wd, q));
-                            F2 f = fma2(nc2, get_pair<C>(ws, q), tq);
-                            if constexpr (DH) f = add2(f, get_pair<C>(we, q));
-                            put_pair<C>(wo, q, f);
-                        }
-                        const int64_t off = int64_t(col) * sizeof(T);
-                        Access<16>::store(dxr + off, wo);
-                        if (drr) Access<16>::store(drr + off, wo);
                     }
                 }
             }
+            __syncwarp();
+            if constexpr (PROD) {
+                // this warp is done with stage s
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            } else {
+                // count this warp out of stage s; the warp that completes the count refills it
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence_block();      // this warp's reads of the stage before its count
+                    last = (atomicAdd(&done[s], 1) + 1) % warps == 0;
+                    if (last) __threadfence_block();   // every other warp's count before the refill
+                }
+                if (__shfl_sync(0xFFFFFFFFu, last, 0) && it + S < iters) issue(it + S);
+            }
         }
-        // count this warp out of stage s; the warp that completes the count refills it
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            __threadfence_block();      // this warp's reads of the stage before its count
-            last = (atomicAdd(&done[s], 1) + 1) % warps == 0;
-            if (last) __threadfence_block();   // every other warp's count before the refill
-        }
-        if (__shfl_sync(0xFFFFFFFFu, last, 0) && it + S < iters) issue(it + S);
     }
     if (__syncthreads_or(failed)) {
         if (threadIdx.x == 0) {
             atomicAdd(&g_rms_timeouts, 1u);
-            // the block may only end once every copy it issued has landed
-            for (int s = 0; s < S; ++s) {
-                const int j = last_issued[s];
-                if (j >= 0 && !mbar_wait_sleep(smem_u32(&full[s]), uint32_t((j / S) & 1))) break;
+            // the block may only end once every copy it issued has landed (the
+            // producer warp has already waited for its own)
+            if constexpr (!PROD) {
+                for (int s = 0; s < S; ++s) {
+                    const int j = last_issued[s];
+                    if (j >= 0 && !mbar_wait_sleep(smem_u32(&full[s]), uint32_t((j / S) & 1))) break;
+                }
             }
         }
         return;
@@ -703,6 +747,7 @@ __global__ void __launch_bounds__(kRmsBwdThreads, 1)
 #pragma unroll
     for (int i = 0; i < NV * QV; ++i) dgf[2 * i] = dg[i].x, dgf[2 * i + 1] = dg[i].y;
     // every copy has landed and been read: the ring is free for the team sums
+    // (a producer warp's partial sums are zero)
     add_dgamma<V, NV>(p.dgamma, p.H, TM, dgf, column, reinterpret_cast<float *>(ring));
 }
 
@@ -770,27 +815,28 @@ __global__ void __launch_bounds__(1024)
 using BwdFn = void (*)(BwdParams);
 
 template <class T, bool DH>
-BwdFn pick_staged(int nv)
+BwdFn pick_staged(int nv, bool prod)
 {
-    return nv == 1 ? add_rmsnorm_bwd_staged_kernel<T, DH, 1>
-                   : nv == 2 ? add_rmsnorm_bwd_staged_kernel<T, DH, 2> : add_rmsnorm_bwd_staged_kernel<T, DH, 4>;
+    if (!prod) return add_rmsnorm_bwd_staged_kernel<T, DH, 4, false>;
+    return nv == 1 ? add_rmsnorm_bwd_staged_kernel<T, DH, 1, true>
+                   : nv == 2 ? add_rmsnorm_bwd_staged_kernel<T, DH, 2, true> : add_rmsnorm_bwd_staged_kernel<T, DH, 4, true>;
 }
 
 // nv = 0: the element kernel; 1, 2 or 4: the staged kernel with nv 16-byte
-// accesses per operand per thread
+// accesses per operand per thread, with a producer warp (prod) or without
 template <class T>
-BwdFn pick_bwd_t(int nv, bool dh)
+BwdFn pick_bwd_t(int nv, bool dh, bool prod)
 {
     if (nv == 0) return add_rmsnorm_bwd_kernel<T, 16>;
-    return dh ? pick_staged<T, true>(nv) : pick_staged<T, false>(nv);
+    return dh ? pick_staged<T, true>(nv, prod) : pick_staged<T, false>(nv, prod);
 }
 
-BwdFn pick_bwd(int dtype, int nv, bool dh)
+BwdFn pick_bwd(int dtype, int nv, bool dh, bool prod)
 {
     switch (dtype) {
-    case GLU_F32: return pick_bwd_t<float>(nv, dh);
-    case GLU_F16: return pick_bwd_t<__half>(nv, dh);
-    default: return pick_bwd_t<__nv_bfloat16>(nv, dh);
+    case GLU_F32: return pick_bwd_t<float>(nv, dh, prod);
+    case GLU_F16: return pick_bwd_t<__half>(nv, dh, prod);
+    default: return pick_bwd_t<__nv_bfloat16>(nv, dh, prod);
     }
 }
 
@@ -960,20 +1006,24 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
         if (pe != cudaSuccess) return glu::cuda_fail(pe);
         staged = dev_mem;
     }
-    // 16-byte rows: NV accesses per operand per thread, the fewest that keep a
-    // row within 512 threads; otherwise 16 elements per thread
-    const int nv = !staged ? 0 : n_cols <= int64_t(512) * V ? 1 : n_cols <= int64_t(1024) * V ? 2 : 4;
+    // 16-byte rows: rows of up to 1024 vectors take the staged kernel with a
+    // producer warp and 256 consumer threads, NV (1, 2 or 4) the fewest
+    // accesses per operand per thread that keep a row within them; wider rows
+    // take it with 512 threads and NV = 4.  Otherwise 16 elements per thread.
+    const bool prod = staged && n_cols <= int64_t(1024) * V;
+    const int nv = !staged ? 0 : n_cols <= int64_t(256) * V ? 1 : n_cols <= int64_t(512) * V ? 2 : 4;
     const int ept = staged ? nv * V : 16;
     int tpr = int((n_cols + ept - 1) / ept);
     tpr = (tpr + 31) / 32 * 32;
     // several rows per block for narrow rows, so that fewer blocks add to
-    // dgamma: the staged kernel's teams fill 512 threads (at most 8 teams of
-    // several warps, one named barrier each, or 16 single-warp teams), the
-    // element kernel up to 512
-    const int groups = tpr >= 512 ? 1 : (512 / tpr < 16 ? 512 / tpr : 16);
-    const int threads = tpr * groups;
-    const int rows_per_stage = staged ? groups * (4 / nv) : groups;
-    BwdFn fn = pick_bwd(dtype, nv, dh != nullptr);
+    // dgamma: the staged kernel's teams fill its consumer threads (at most 8
+    // teams of several warps, one named barrier each, or single-warp teams),
+    // the element kernel up to 512 threads
+    const int team_threads = prod ? kRmsBwdConsumersP : kRmsBwdThreads;
+    const int groups = tpr >= team_threads ? 1 : (team_threads / tpr < 16 ? team_threads / tpr : 16);
+    const int threads = tpr * groups + (prod ? 32 : 0);
+    const int rows_per_stage = staged ? groups * ((prod ? 8 : 4) / nv) : groups;
+    BwdFn fn = pick_bwd(dtype, nv, dh != nullptr, prod);
 
     int dev = 0, sms = 0, smem_sm = 0, smem_block = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -992,9 +1042,9 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
         // fits, 8 at most.  A stage holds at most 512 x 64 bytes per operand,
         // 96 KiB for three, so at least 2 fit.
         // per device and kernel: the shared-memory limit raised once
-        static std::atomic<int> opted[64][18];
+        static std::atomic<int> opted[64][24];
         std::atomic<int> &flag = opted[dev % 64][((dtype == GLU_F32 ? 0 : dtype == GLU_F16 ? 1 : 2) * 2 +
-                                                   (dh != nullptr)) * 3 + (nv == 4 ? 2 : nv - 1)];
+                                                   (dh != nullptr)) * 4 + (prod ? (nv == 4 ? 2 : nv - 1) : 3)];
         if (!flag.load(std::memory_order_acquire)) {
             e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      smem_block);
@@ -1005,7 +1055,7 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
             flag.store(1, std::memory_order_release);
         }
         const size_t stage = size_t(rows_per_stage) * (dh ? 3 : 2) * size_t(n_cols) * E;
-        const size_t per_stage = stage + 8 + 2 * sizeof(int) + size_t(rows_per_stage) * sizeof(float);
+        const size_t per_stage = stage + 16 + size_t(rows_per_stage) * sizeof(float);   // rows, 2 x 8 B, rstd
         const size_t fixed =
             2 * size_t(rows_per_stage) * (tpr / 32) * sizeof(float) + 2 * size_t(groups) * sizeof(int);
         const int64_t room = int64_t(smem_sm) - 1024 < int64_t(smem_block) ? int64_t(smem_sm) - 1024

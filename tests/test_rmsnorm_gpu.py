@@ -249,8 +249,8 @@ def test_bwd_parity(orc, shape, dt):
         vec = (H * E) % 16 == 0 and H <= 2048 * V
         assert info["backward"] == 1 and info["vec_bytes"] == (16 if vec else E) and info["grid"] <= rows
         # 16-byte rows: the fewest 16-byte accesses per operand per thread (1, 2 or 4) that keep a row
-        # within 512 threads
-        nv = 1 if H <= 512 * V else 2 if H <= 1024 * V else 4
+        # within the 256 consumer threads beside the producer warp; wider rows 4 at 512 threads
+        nv = 1 if H <= 256 * V else 2 if H <= 512 * V else 4
         assert info["unroll"] == (nv * V if vec else 16)
         assert glu.glu_wait_timeouts() == 0
         check_bwd(orc, dt, dy, h, rstd, g, dh, dx, dg, f"bwd {dt} {shape} dh={with_dh}")
