@@ -230,10 +230,13 @@ def run_bwd(dy, h, rstd, g, dh, dt, dres=False, dgamma=True):
 
 
 TORCH_INT_OF = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}
-# (30011, 64) and (6000, 1024): blocks of 16 and 4 rows that go round the
-# shared-memory ring of the 16-byte path several times, the last group ragged
+# (30011, 64) and (6000, 1024): stages that go round the shared-memory ring
+# of the 16-byte path several times, the last one ragged; (9, 5000): a
+# 160-thread team beside the producer warp; (33, 8200): just past 1024
+# vectors a row (16-bit types), the kernel without a producer warp on a
+# 288-thread team
 BWD_SHAPES = [(1, 1), (3, 7), (5, 64), (77, 100), (33, 1000), (64, 4096), (9, 5000), (17, 8192), (4, 16384),
-              (513, 1536), (30011, 64), (6000, 1024)]
+              (513, 1536), (30011, 64), (6000, 1024), (33, 8200)]
 
 
 @pytest.mark.parametrize("dt", DTYPES)
