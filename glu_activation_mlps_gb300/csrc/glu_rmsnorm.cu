@@ -17,10 +17,16 @@
 //
 // Rows whose operands are 16-byte aligned (bases, strides and row width) use
 // 16-byte accesses, element i of a thread's k-th vector at column
-// (t + k * threads) * V + i, in a persistent grid (add_rmsnorm_rows_kernel);
-// other rows use element accesses at column t + k * threads, one block per row
-// (add_rmsnorm_kernel).  Either way consecutive threads touch consecutive
-// addresses.
+// (t + k * threads) * V + i: rows of 16 KiB or more in a persistent grid
+// (add_rmsnorm_rows_kernel), narrower ones one block per row
+// (add_rmsnorm_kernel); other rows use element accesses at column
+// t + k * threads, one block per row.  Either way consecutive threads touch
+// consecutive addresses.
+//
+// The backward (glu_add_rmsnorm_bwd, below the forward) has two kernels:
+// add_rmsnorm_bwd_staged_kernel for 16-byte rows in device memory (rows staged
+// in shared memory by the bulk-copy engine) and add_rmsnorm_bwd_kernel with
+// element accesses for the rest.
 #include <cuda_runtime.h>
 
 #include <atomic>
