@@ -12,6 +12,12 @@ add eps, square root and reciprocal), y 2 more, in all at most 14.5 * 2^-24 =
 Shapes cover 16-byte-vector rows (widths that are multiples of 16 bytes) and
 element rows (odd widths, misaligned bases), 16 and 64 elements per thread,
 one-warp and 1024-thread blocks, in-place updates and padded strides.
+
+The backward (glu_add_rmsnorm_bwd) is held to a bound derived from its fp32
+arithmetic (check_bwd) on the same kinds of rows: the staged kernel with a
+producer warp (up to 1024 16-byte vectors a row) and without one (wider
+rows), the element kernel, ragged stages, in place, a second output, and
+pinned host inputs.
 """
 import numpy as np
 import pytest
