@@ -179,8 +179,9 @@ cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, vo
 int plan_direct(const Call &c, cudaStream_t stream);
 
 // Bulk-copy staging path: contiguous operands, 16-byte aligned, inputs in
-// device memory, at least one whole chunk.  Whole chunks go to the bulk kernel (one block per SM), the
-// remainder to the direct kernel.  Returns 1 if the call is not eligible.
+// device memory, at least one whole chunk.  Whole chunks go to the bulk kernel
+// (one block per SM), the remainder to the direct kernel.  Returns 1 if the
+// call is not eligible.
 int plan_bulk(const Call &c, cudaStream_t stream)
 {
     const int n_ops = c.dir == kBwd ? 5 : 3;
