@@ -644,7 +644,9 @@ const char *glu_status_string(int status)
     case GLU_ERR_ENUM: return "unknown activation, layout, dtype or tuning value";
     case GLU_ERR_CUDA: return "the CUDA runtime refused a launch or copy";
     case GLU_ERR_WORKSPACE: return "the workspace is NULL or too small for one row";
-    case GLU_ERR_VALUE: return "an argument is out of range (eps not finite and > 0, or a GEMM operand or dgamma not in device memory)";
+    case GLU_ERR_VALUE:
+        return "an argument is out of range (eps not finite and > 0, or a GEMM operand or dgamma not in device "
+               "memory)";
     default: return "unknown status";
     }
 }

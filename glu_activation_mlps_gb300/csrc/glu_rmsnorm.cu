@@ -824,8 +824,9 @@ template <class T, bool DH>
 BwdFn pick_staged(int nv, bool prod)
 {
     if (!prod) return add_rmsnorm_bwd_staged_kernel<T, DH, 4, false>;
-    return nv == 1 ? add_rmsnorm_bwd_staged_kernel<T, DH, 1, true>
-                   : nv == 2 ? add_rmsnorm_bwd_staged_kernel<T, DH, 2, true> : add_rmsnorm_bwd_staged_kernel<T, DH, 4, true>;
+    return nv == 1   ? add_rmsnorm_bwd_staged_kernel<T, DH, 1, true>
+           : nv == 2 ? add_rmsnorm_bwd_staged_kernel<T, DH, 2, true>
+                     : add_rmsnorm_bwd_staged_kernel<T, DH, 4, true>;
 }
 
 // nv = 0: the element kernel; 1, 2 or 4: the staged kernel with nv 16-byte
