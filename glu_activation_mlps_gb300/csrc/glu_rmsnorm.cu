@@ -757,6 +757,113 @@ __global__ void __launch_bounds__(PROD ? kRmsBwdConsumersP + 32 : kRmsBwdThreads
     add_dgamma<V, NV>(p.dgamma, p.H, TM, dgf, column, reinterpret_cast<float *>(ring));
 }
 
+// Narrow 16-byte rows (up to 128 vectors, 1024 elements of 16-bit types):
+// the persistent staged kernel would give each block fewer than two stages,
+// so its fill and drain, and a launch the next one cannot overlap, decide the
+// time.  This kernel is not persistent: a block of 256 threads takes 4 rows
+// for each of its teams (one 16-byte access per operand per thread), loads
+// them straight into registers, forms the row sums (a warp reduction and the
+// team's named barrier), writes ds from the same registers and adds the
+// block's dgamma partial sums once, with 16-byte reductions.  A block holds
+// 4.2 KiB of shared memory and at most 128 registers a thread: two per SM.
+constexpr int kRmsBwdNarrowThreads = 256;
+constexpr int kRmsBwdNarrowRows = 4;        // rows per team
+
+template <class T, bool DH>
+__global__ void __launch_bounds__(kRmsBwdNarrowThreads, 2)
+    add_rmsnorm_bwd_narrow_kernel(const BwdParams p)
+{
+    using C = Codec<T>;
+    constexpr int V = 16 / int(sizeof(T));      // elements per 16-byte access
+    constexpr int QV = V / 2;                   // element pairs per access
+    constexpr int R = kRmsBwdNarrowRows;
+    constexpr int W = 4;
+    __shared__ float red[kRmsBwdNarrowThreads / 32 * R];          // [team][R][warps of the team]: 32
+    __shared__ float dgs[1024];                                   // the teams' dgamma partial sums
+    const int TM = p.groups, tpr = p.tpr, nwg = tpr >> 5;
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const int lane = threadIdx.x & 31;
+    const int t = threadIdx.x / tpr, tg = threadIdx.x - t * tpr, wig = tg >> 5;
+    const int col = tg * V;
+    const bool on_col = t < TM && col < p.H;
+    const int64_t row0 = (int64_t(blockIdx.x) * TM + t) * R;
+
+    uint32_t gw[W] = {0, 0, 0, 0};
+    if (on_col) Access<16>::load(p.gamma + int64_t(col) * sizeof(T), gw);
+    // every row of this thread's team, loaded before any arithmetic
+    uint32_t wd[R][W], ws[R][W];
+    float rs[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = row0 + r;
+        const bool on = on_col && row < p.rows;
+        rs[r] = on ? p.rstd[row] : 0.0f;
+        if (on) {
+            Access<16>::load(p.dy + row * p.sdy + int64_t(col) * sizeof(T), wd[r]);
+            Access<16>::load(p.h + row * p.sh + int64_t(col) * sizeof(T), ws[r]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) wd[r][j] = ws[r][j] = 0;
+        }
+    }
+    F2 dg[QV];
+#pragma unroll
+    for (int q = 0; q < QV; ++q) dg[q] = F2{0.0f, 0.0f};
+    float tot[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        F2 dot{0.0f, 0.0f};
+        const F2 rs2{rs[r], rs[r]};
+#pragma unroll
+        for (int q = 0; q < QV; ++q) {
+            const F2 ds = mul2(get_pair<C>(wd[r], q), get_pair<C>(ws[r], q));
+            dg[q] = fma2(ds, rs2, dg[q]);
+            dot = fma2(get_pair<C>(gw, q), ds, dot);
+        }
+        tot[r] = warp_sum(dot.x + dot.y);
+    }
+    if (nwg > 1) {
+        float *rr = red + t * R * nwg;
+        if (lane == 0 && t < TM) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) rr[r * nwg + wig] = tot[r];
+        }
+        if (t < TM) named_barrier(1 + t, tpr);
+#pragma unroll
+        for (int r = 0; r < R; ++r) tot[r] = warp_sum(lane < nwg && t < TM ? rr[r * nwg + lane] : 0.0f);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = row0 + r;
+        if (!on_col || row >= p.rows) continue;
+        const float c = rs[r] * rs[r] * rs[r] * (tot[r] / float(p.H));
+        const F2 nc2{-c, -c}, rs2{rs[r], rs[r]};
+        uint32_t we[W] = {0, 0, 0, 0};
+        if constexpr (DH) Access<16>::load(p.dh + row * p.sdh + int64_t(col) * sizeof(T), we);
+        uint32_t wo[W];
+#pragma unroll
+        for (int q = 0; q < QV; ++q) {
+            // rs * gamma * d - c * s (+ dh)
+            const F2 tq = mul2(mul2(rs2, get_pair<C>(gw, q)), get_pair<C>(wd[r], q));
+            F2 f = fma2(nc2, get_pair<C>(ws[r], q), tq);
+            if constexpr (DH) f = add2(f, get_pair<C>(we, q));
+            put_pair<C>(wo, q, f);
+        }
+        const int64_t off = int64_t(col) * sizeof(T);
+        Access<16>::store(p.dx + row * p.sdx + off, wo);
+        if (p.dres) Access<16>::store(p.dres + row * p.sdr + off, wo);
+    }
+    if (!p.dgamma) return;
+    float dgf[V];
+#pragma unroll
+    for (int q = 0; q < QV; ++q) dgf[2 * q] = dg[q].x, dgf[2 * q + 1] = dg[q].y;
+    // threads outside every team hold zeros; their columns are valid ones
+    add_dgamma<V, 1>(p.dgamma, p.H, TM, dgf, [&](int) { return on_col ? col : 0; }, dgs);
+}
+
 // Rows that are not 16-byte aligned: the same arithmetic with element
 // accesses, each thread owning EPT columns t + k * tpr, one load of each
 // element per pass (the second pass's loads hit the cache).
@@ -836,6 +943,18 @@ BwdFn pick_bwd_t(int nv, bool dh, bool prod)
 {
     if (nv == 0) return add_rmsnorm_bwd_kernel<T, 16>;
     return dh ? pick_staged<T, true>(nv, prod) : pick_staged<T, false>(nv, prod);
+}
+
+BwdFn pick_narrow(int dtype, bool dh)
+{
+    switch (dtype) {
+    case GLU_F32: return dh ? add_rmsnorm_bwd_narrow_kernel<float, true> : add_rmsnorm_bwd_narrow_kernel<float, false>;
+    case GLU_F16:
+        return dh ? add_rmsnorm_bwd_narrow_kernel<__half, true> : add_rmsnorm_bwd_narrow_kernel<__half, false>;
+    default:
+        return dh ? add_rmsnorm_bwd_narrow_kernel<__nv_bfloat16, true>
+                  : add_rmsnorm_bwd_narrow_kernel<__nv_bfloat16, false>;
+    }
 }
 
 BwdFn pick_bwd(int dtype, int nv, bool dh, bool prod)
@@ -1017,21 +1136,6 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     // producer warp and 256 consumer threads, NV (1, 2 or 4) the fewest
     // accesses per operand per thread that keep a row within them; wider rows
     // take it with 512 threads and NV = 4.  Otherwise 16 elements per thread.
-    const bool prod = staged && n_cols <= int64_t(1024) * V;
-    const int nv = !staged ? 0 : n_cols <= int64_t(256) * V ? 1 : n_cols <= int64_t(512) * V ? 2 : 4;
-    const int ept = staged ? nv * V : 16;
-    int tpr = int((n_cols + ept - 1) / ept);
-    tpr = (tpr + 31) / 32 * 32;
-    // several rows per block for narrow rows, so that fewer blocks add to
-    // dgamma: the staged kernel's teams fill its consumer threads (at most 8
-    // teams of several warps, one named barrier each, or single-warp teams),
-    // the element kernel up to 512 threads
-    const int team_threads = prod ? kRmsBwdConsumersP : kRmsBwdThreads;
-    const int groups = tpr >= team_threads ? 1 : (team_threads / tpr < 16 ? team_threads / tpr : 16);
-    const int threads = tpr * groups + (prod ? 32 : 0);
-    const int rows_per_stage = staged ? groups * ((prod ? 8 : 4) / nv) : groups;
-    BwdFn fn = pick_bwd(dtype, nv, dh != nullptr, prod);
-
     int dev = 0, sms = 0, smem_sm = 0, smem_block = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1041,9 +1145,37 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
         (void)cudaGetLastError();
         return glu::cuda_fail(e);
     }
+    // Rows of up to 128 vectors take the non-persistent narrow kernel instead
+    // (4 rows per team, one access per operand per thread) when its grid fits
+    // on the GPU at once (two blocks per SM): every block adds to dgamma, and
+    // more blocks than that queue their additions on the same addresses
+    // (measured: 262144 rows of 64 took 2.5 times the persistent kernel's time).
+    const int64_t narrow_tpr = ((n_cols + V - 1) / V + 31) / 32 * 32;
+    const int64_t narrow_rows = kRmsBwdNarrowThreads / narrow_tpr * kRmsBwdNarrowRows;
+    const bool narrow = staged && n_cols <= int64_t(128) * V &&
+                        (n_rows + narrow_rows - 1) / narrow_rows <= 2 * int64_t(sms);
+    const bool prod = staged && !narrow && n_cols <= int64_t(1024) * V;
+    const int nv = !staged ? 0 : n_cols <= int64_t(256) * V ? 1 : n_cols <= int64_t(512) * V ? 2 : 4;
+    const int ept = staged ? nv * V : 16;
+    int tpr = int((n_cols + ept - 1) / ept);
+    tpr = (tpr + 31) / 32 * 32;
+    // several rows per block for narrow rows, so that fewer blocks add to
+    // dgamma: the staged kernel's teams fill its consumer threads (at most 8
+    // teams of several warps, one named barrier each, or single-warp teams),
+    // the element kernel up to 512 threads
+    const int team_threads = narrow ? kRmsBwdNarrowThreads : prod ? kRmsBwdConsumersP : kRmsBwdThreads;
+    const int groups = tpr >= team_threads ? 1 : (team_threads / tpr < 16 ? team_threads / tpr : 16);
+    const int threads = narrow ? kRmsBwdNarrowThreads : tpr * groups + (prod ? 32 : 0);
+    const int rows_per_stage = narrow   ? groups * kRmsBwdNarrowRows
+                               : staged ? groups * ((prod ? 8 : 4) / nv)
+                                        : groups;
+    BwdFn fn = narrow ? pick_narrow(dtype, dh != nullptr) : pick_bwd(dtype, nv, dh != nullptr, prod);
+
     size_t smem = sizeof(float) * (size_t(2 * groups * 33) + (groups > 1 ? size_t(n_cols) : 0));
     int stages = 0, per_sm = 1;
-    if (staged) {
+    if (narrow) {
+        smem = 0;       // static shared memory only
+    } else if (staged) {
         // One block per SM with the deepest ring of stages (dy, h and dh rows,
         // the mbarrier, last issued stage, counter and rstd values) that
         // fits, 8 at most.  A stage holds at most 512 x 64 bytes per operand,
@@ -1080,7 +1212,8 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     }
     const int64_t slots = int64_t(sms) * per_sm;
     const int64_t want = (n_rows + rows_per_stage - 1) / rows_per_stage;
-    const int64_t blocks = want < slots ? want : slots;
+    // the narrow kernel is not persistent: one block per row group
+    const int64_t blocks = narrow ? (want < int64_t(INT32_MAX) ? want : int64_t(INT32_MAX)) : want < slots ? want : slots;
 
     BwdParams p{};
     p.dy = static_cast<const char *>(dy);
