@@ -23,10 +23,11 @@
 // t + k * threads, one block per row.  Either way consecutive threads touch
 // consecutive addresses.
 //
-// The backward (glu_add_rmsnorm_bwd, below the forward) has two kernels:
+// The backward (glu_add_rmsnorm_bwd, below the forward) has three kernels:
 // add_rmsnorm_bwd_staged_kernel for 16-byte rows in device memory (rows staged
-// in shared memory by the bulk-copy engine) and add_rmsnorm_bwd_kernel with
-// element accesses for the rest.
+// in shared memory by the bulk-copy engine), add_rmsnorm_bwd_narrow_kernel for
+// narrow 16-byte rows when its grid fits on the GPU at once, and
+// add_rmsnorm_bwd_kernel with element accesses for the rest.
 #include <cuda_runtime.h>
 
 #include <atomic>
