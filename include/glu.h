@@ -424,10 +424,12 @@ int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride,
  *
  * Rows whose operands are 16-byte aligned (bases, strides, width) and whose
  * inputs dy, h, dh and rstd are in device memory are staged in shared memory
- * by the bulk-copy engine; every wait there is bounded (about a second) and
- * one that runs out is counted by glu_wait_timeouts() and leaves that launch's
- * outputs and dgamma incomplete.  Other rows (pinned host inputs included)
- * use element accesses.
+ * by the bulk-copy engine, except narrow rows (up to 128 16-byte vectors) in
+ * a launch small enough to fit on the GPU at once, which are loaded straight
+ * into registers.  Every wait of the staged kernel is bounded (about a
+ * second); one that runs out is counted by glu_wait_timeouts() and leaves
+ * that launch's outputs and dgamma incomplete.  Other rows (pinned host
+ * inputs included) use element accesses.
  */
 int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride,
                         const void *h, int64_t h_stride,
