@@ -582,6 +582,114 @@ def run_table(args):
               flush=True)
 
 
+# ---------------------------------------------------------------- one workload at a time (ncu captures)
+
+CASES = {
+    # name: (generator, dir, act, layout, in place, description)
+    "c1": ("fwd_f32_small", "fwd", "silu", "split", False, "SwiGLU fwd f32 256x1024"),
+    "c2": ("fwd_bf16_split", "fwd", "silu", "split", False, "SwiGLU fwd bf16 4096x11008"),
+    "c3": ("fwd_bf16_concat", "fwd", "silu", "concat", False, "SwiGLU fwd bf16 [gate|up] 4096x(2x18944)"),
+    "c3_inplace": ("fwd_bf16_concat", "fwd", "silu", "concat", True,
+                   "SwiGLU fwd bf16 [gate|up] 4096x(2x18944), y over the up half"),
+    "c4": ("bwd_bf16_outliers", "bwd", "silu", "split", True, "SwiGLU bwd bf16 4096x28672, da->a, db->b"),
+    "metric_fwd": ("metric_bf16", "fwd", "silu", "split", False, "SwiGLU fwd bf16 4096x14336"),
+    "metric_bwd": ("metric_bf16", "bwd", "silu", "split", False, "SwiGLU bwd bf16 4096x14336"),
+}
+
+
+def case_data(name):
+    """Inputs (host bit arrays) and the call's description for a named
+    workload, or for `sweep:<act>:<dtype>:<fwd|bwd>:<H>` (a 4096 x H case of
+    the activation sweep)."""
+    if name.startswith("sweep:"):
+        _, act, dt, direction, H = name.split(":")
+        d = glu_synth.sweep(int(H), dt, with_dc=direction == "bwd")
+        return d, direction, act, "split", False, f"{act} {direction} {dt} 4096x{H}"
+    if name not in CASES:
+        raise SystemExit(f"unknown case {name!r}: one of {', '.join(CASES)} or sweep:<act>:<dtype>:<dir>:<H>")
+    gen, direction, act, layout, inplace, desc = CASES[name]
+    return getattr(glu_synth, gen)(), direction, act, layout, inplace, desc
+
+
+def run_case(args):
+    """One named workload launched --warmup + --steps times, each launch timed
+    with CUDA events on its stream; in-place cases restore their inputs before
+    every launch, outside the timed pair.  This is the command the per-config
+    ncu captures profile (`-k regex:glu_kernel -s <warmup> -c 1`).  Prints one
+    JSON line (not the benchmark's line)."""
+    import torch
+    import glu_activation_mlps_gb300 as glu
+
+    glu.build()
+    L = glu.lib()
+    glu.glu_set_tuning(path={"default": 0, "direct": 1, "bulk": 2}[args.path])
+    d, direction, act, layout, inplace, desc = case_data(args.case)
+    dt = d["dtype"]
+    E_ = glu_synth.ELEM_BYTES[dt]
+    code, a_ = glu.DTYPE[dt], glu.ACT[act]
+    dev = torch.device("cuda", 0)
+    sh = torch.cuda.current_stream(dev).cuda_stream
+
+    def put(x):
+        return torch.from_numpy(x.view(np.int32 if x.dtype == np.uint32 else np.int16)).to(dev)
+
+    keep = []          # (live tensor, pristine copy) pairs restored before each launch
+    if layout == "concat":
+        X = put(d["x"])
+        R, C = X.shape[0], d["n_cols"]
+        Y = X[:, C:] if inplace else torch.empty(R, C, dtype=X.dtype, device=dev)
+        ys = 2 * C if inplace else C
+        if inplace:
+            keep.append((X, X.clone()))
+
+        def launch():
+            return L.glu_fwd(X.data_ptr(), 2 * C, None, 0, Y.data_ptr(), ys, R, C, glu.LAYOUT["concat"], a_, code, sh)
+    else:
+        A, B = put(d["a"]), put(d["b"])
+        R, C = A.shape
+        if direction == "fwd":
+            Y = torch.empty_like(A)
+
+            def launch():
+                return L.glu_fwd(A.data_ptr(), C, B.data_ptr(), C, Y.data_ptr(), C, R, C, 0, a_, code, sh)
+        else:
+            DC = put(d["dc"])
+            DA, DB = (A, B) if inplace else (torch.empty_like(A), torch.empty_like(B))
+            if inplace:
+                keep += [(A, A.clone()), (B, B.clone())]
+
+            def launch():
+                return L.glu_bwd(DC.data_ptr(), C, A.data_ptr(), C, B.data_ptr(), C, DA.data_ptr(), C,
+                                 DB.data_ptr(), C, R, C, 0, a_, code, sh)
+    del d
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    info = None
+    for k in range(args.warmup + args.steps):
+        for live, pristine in keep:
+            live.copy_(pristine)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = launch()
+        e1.record(stream)
+        if st:
+            raise glu.GluError(st, "case launch")
+        info = dict(glu.glu_last_launch())
+        if k >= args.warmup:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in times]
+    nbytes = (3 if direction == "fwd" else 5) * E_ * R * C
+    peak, src = measured_peak()
+    med = statistics.median(us)
+    print(json.dumps({"case": args.case, "what": desc, "rows": R, "cols": C, "dtype": dt, "act": act,
+                      "dir": direction, "in_place": inplace, "algorithmic_bytes": nbytes,
+                      "launches": args.warmup + args.steps, "timed": len(us),
+                      "us_median": round(med, 3), "us_min": round(min(us), 3),
+                      "gbs": round(nbytes / med / 1e3, 1), "frac_of_copy": round(nbytes / med / 1e3 / peak, 4),
+                      "peak_source": src, "launch": info}), flush=True)
+
+
 # ---------------------------------------------------------------- gate/up GEMM with the activation in the epilogue
 
 GM, GK, GI = 4096, 4096, 14336      # tokens, hidden size, intermediate size of one MLP layer
@@ -940,9 +1048,16 @@ def main():
     ap.add_argument("--path", default="default", choices=["default", "direct", "bulk"],
                     help="load path of the kernels (library default, direct loads, or bulk copies "
                          "staged in shared memory); for profiling and comparisons")
+    ap.add_argument("--case", default=None,
+                    help="launch one named workload (" + ", ".join(CASES) + ", or sweep:<act>:<dtype>:<dir>:<H>) "
+                         "--warmup + --steps times and print its per-launch time (the command the per-config "
+                         "ncu captures profile)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.case:
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

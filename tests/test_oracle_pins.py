@@ -225,6 +225,98 @@ def test_against_literal_page_formulas_at_high_precision(orc):
         assert np.max(np.abs((t1 + t2) - dwant) / (np.abs(t1) + np.abs(t2))) < 1e-12, name
 
 
+# the gate factor g of act(x) = x * g(x), as the pages print it, at high precision
+def _gate_factors(mp):
+    k, c = mp.mpf("0.044715"), mp.sqrt(2 / mp.pi)
+    return {
+        "silu": lambda x: 1 / (1 + mp.exp(-x)),                          # sigmoid
+        "gelu_erf": lambda x: (1 + mp.erf(x / mp.sqrt(2))) / 2,          # Phi
+        "gelu_tanh": lambda x: (1 + mp.tanh(c * (x + k * x ** 3))) / 2,
+    }
+
+
+def _split_points(name):
+    roots = {"silu": -1.2784645427610738, "gelu_erf": -0.7517915246935645, "gelu_tanh": -0.7524614}
+    lo = {"silu": -60.0, "gelu_erf": -12.0, "gelu_tanh": -11.0}[name]
+    r = roots[name]
+    return np.concatenate([np.linspace(lo, 12, 173), r + np.linspace(-1e-3, 1e-3, 11), [1e-9, -1e-9, 0.0]])
+
+
+@pytest.mark.parametrize("name", ["silu", "gelu_erf", "gelu_tanh"])
+def test_act_grad_terms_one_by_one(orc, name):
+    """The oracle splits act'(x) of act(x) = x g(x) into t1 = g(x) and
+    t2 = x g'(x) (product rule), and the fp32 tolerance of da scales with
+    |t1| + |t2|.  Each term on its own, not only their sum, must equal the
+    printed gate factor and x times its derivative, both evaluated here at
+    60 digits with g' taken by mpmath's numerical differentiation of the
+    printed g: sigmoid and x sigmoid(x) sigmoid(-x) for SiLU, Phi and x phi for
+    GeGLU-erf, the tanh-form factor and x times its slope for GeGLU-tanh
+    ("Kernel Profile: SwiGLU (Tier 1 - Element-wise)", Backward Pass,
+    gradient formulas; "Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel",
+    Required reasoning process step 7).  A term moved from one side to the
+    other, swapped or offset by a constant keeps the sum and fails here."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 60
+    g = _gate_factors(mp)[name]
+    xs = _split_points(name)
+    want1 = np.array([float(g(mp.mpf(float(x)))) for x in xs])
+    want2 = np.array([float(mp.mpf(float(x)) * mp.diff(g, mp.mpf(float(x)))) for x in xs])
+    t1, t2 = orc.act_grad_terms(name, xs)
+    assert np.max(np.abs(t1 - want1) / np.abs(want1)) < 1e-13, name
+    nz = want2 != 0.0
+    assert np.all(t2[~nz] == 0.0), name
+    assert np.max(np.abs(t2[nz] - want2[nz]) / np.abs(want2[nz])) < 1e-12, name
+
+
+def test_act_grad_terms_closed_values():
+    """Closed forms of the split that need no numerical differentiation:
+    SiLU at 0 is (1/2, 0); GeGLU-erf at 1 is (Phi(1), phi(1)) with
+    Phi(1) = erfc(-1/sqrt 2)/2 and phi(1) = exp(-1/2)/sqrt(2 pi) (the
+    standard normal CDF and density, here from scipy's ndtr and the textbook
+    density); SiLU's t2 at x = ln 3 is ln 3 * (3/4) * (1/4); ReGLU's t2 is 0
+    everywhere."""
+    import oracle
+    from scipy.special import ndtr
+    t1, t2 = oracle.act_grad_terms("silu", [0.0, math.log(3.0)])
+    assert (t1[0], t2[0]) == (0.5, 0.0)
+    assert t1[1] == pytest.approx(0.75, rel=1e-15)
+    assert t2[1] == pytest.approx(math.log(3.0) * 0.75 * 0.25, rel=1e-15)
+    t1, t2 = oracle.act_grad_terms("gelu_erf", [1.0, -2.0])
+    assert t1[0] == pytest.approx(ndtr(1.0), rel=1e-15)
+    assert t2[0] == pytest.approx(math.exp(-0.5) / math.sqrt(2 * math.pi), rel=1e-15)
+    assert t1[1] == pytest.approx(ndtr(-2.0), rel=1e-14)
+    assert t2[1] == pytest.approx(-2.0 * math.exp(-2.0) / math.sqrt(2 * math.pi), rel=1e-15)
+    x = np.array([-3.0, -0.0, 0.5, 7.0])
+    t1, t2 = oracle.act_grad_terms("relu", x)
+    assert list(t1) == [0.0, 0.0, 1.0, 1.0] and not np.any(t2)
+
+
+@pytest.mark.parametrize("name", ACTS)
+def test_bwd_da_scale_from_independent_terms(orc, name):
+    """bwd_da_scale(dc, a, b) = |dc b| (|t1(a)| + |t2(a)|), rebuilt here from
+    terms computed outside the oracle (mpmath as above; ReGLU: 1[a > 0], 0)
+    on decoded bf16 inputs, every sign combination of dc and b included."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    rng = np.random.default_rng(11)
+    n = 96
+    a = glu_synth.normal_bits(rng, n, 2.0, "bf16")
+    b = glu_synth.normal_bits(rng, n, 1.0, "bf16")
+    dc = glu_synth.normal_bits(rng, n, 1.0, "bf16")
+    av, bv, cv = (orc.decode("bf16", v) for v in (a, b, dc))
+    if name == "relu":
+        m1, m2 = (av > 0).astype(np.float64), np.zeros(n)
+    else:
+        g = _gate_factors(mp)[name]
+        m1 = np.array([float(g(mp.mpf(float(x)))) for x in av])
+        m2 = np.array([float(mp.mpf(float(x)) * mp.diff(g, mp.mpf(float(x)))) for x in av])
+    want = np.abs(cv * bv) * (np.abs(m1) + np.abs(m2))
+    got = orc.bwd_da_scale(name, "bf16", dc, a, b)
+    assert np.all((got == 0) == (want == 0)), name
+    nz = want != 0
+    assert np.max(np.abs(got[nz] - want[nz]) / want[nz]) < 1e-12, name
+
+
 # --------------------------------------------------------------------------- library routines
 
 @pytest.mark.parametrize("name", ACTS)
