@@ -1,12 +1,14 @@
 """Generates the lower-tail normal-CDF approximations used by the GeGLU-erf
-kernels (the coefficient tables of `phi_tail` in glu_math.cuh): degree 7 for
-bf16 / f16 storage, degree 10 for f32 storage.
+kernels (the coefficient tables of `phi_tail` in glu_math.cuh): degree 4 with
+C = 0.4 for the forward on bf16 / f16 storage, degree 7 with C = 0.3 for the
+backward on bf16 / f16 storage (whose act' amplifies the error of Phi near its
+root), degree 10 with C = 0.3 for f32 storage.
 
 For x >= 0 the lower tail of the standard normal distribution is written as
 
     Phi(-x) = 0.5 * erfc(x / sqrt 2) = exp(-x^2 / 2) * t * P(t),   t = 1 / (1 + C x),
 
-with P a polynomial of degree DEG on t in (0, 1] (both fits use C = 0.3).  P is smooth there: at t = 1
+with P a polynomial of degree DEG on t in (0, 1].  P is smooth there: at t = 1
 (x = 0) it is 1/2, and as t -> 0 (x -> infinity) it tends to C / sqrt(2 pi),
 because Phi(-x) ~ exp(-x^2/2) / (x sqrt(2 pi)) (Mills' ratio).  The exact P is
 evaluated with mpmath; the coefficients minimise the maximum relative error
@@ -62,9 +64,9 @@ def check(coef32):
 
 
 if __name__ == "__main__":
-    print(f"// Phi(-x) = exp(-x^2/2) * t * P(t), t = 1/(1 + {C} x)")
-    for deg, use in ((7, "bf16 / f16 storage"), (10, "f32 storage")):
-        DEG = deg
+    for c, deg, use in ((0.4, 4, "bf16 / f16 forward"), (0.3, 7, "bf16 / f16 backward"), (0.3, 10, "f32 storage")):
+        C, DEG = c, deg
+        print(f"// Phi(-x) = exp(-x^2/2) * t * P(t), t = 1/(1 + {C} x)")
         coef = fit()
         e64, e32 = check(coef)
         print(f"// degree {DEG} ({use}): max relative error of P {e64:.2e} with float32 "

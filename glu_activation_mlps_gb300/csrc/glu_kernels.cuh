@@ -189,6 +189,22 @@ __device__ __forceinline__ void op_bwd(float c, float a, float b, float &da, flo
     db = c * s;                                                // dc * act(a)
 }
 
+// One storage word of the forward (1 or 2 elements): y = act(a) * b; a
+// 16-bit word's two elements as one pair.
+template <class Act, bool Exact, class Cd, int PW = Cd::kPerWord>
+__device__ __forceinline__ void fwd_word(uint32_t wa, uint32_t wb, float (&y)[PW])
+{
+    if constexpr (PW == 2) {
+        const f2 a = make_float2(Cd::get(wa, 0), Cd::get(wa, 1));
+        const f2 b = make_float2(Cd::get(wb, 0), Cd::get(wb, 1));
+        const f2 r = mul2(Act::fwd2(a), b);                    // act(a) * b
+        y[0] = r.x;
+        y[1] = r.y;
+    } else {
+        y[0] = op_fwd<Act, Exact>(Cd::get(wa, 0), Cd::get(wb, 0));
+    }
+}
+
 // One storage word of the backward (1 or 2 elements): act and act' for every
 // element, the root series only on the rare path where an element lies next
 // to a root of act', then da = dc act' b and db = dc act.
@@ -196,23 +212,30 @@ template <class Act, bool Exact, class Cd, int PW = Cd::kPerWord>
 __device__ __forceinline__ void bwd_word(uint32_t wa, uint32_t wb, uint32_t wc, float (&da)[PW],
                                          float (&db)[PW])
 {
-    float a[PW], s[PW], ds[PW];
-    bool near = false;
-#pragma unroll
-    for (int e = 0; e < PW; ++e) {
-        a[e] = Cd::get(wa, e);
-        Act::template bwd_main<Exact>(a[e], &s[e], &ds[e]);
-        near |= Act::near_root(a[e]);
-    }
-    if (near) {
-#pragma unroll
-        for (int e = 0; e < PW; ++e) Act::fix_root(a[e], &ds[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < PW; ++e) {
-        const float c = Cd::get(wc, e), b = Cd::get(wb, e);
-        da[e] = c * ds[e] * b;                                 // dc * act'(a) * b
-        db[e] = c * s[e];                                      // dc * act(a)
+    if constexpr (PW == 2) {
+        const f2 a = make_float2(Cd::get(wa, 0), Cd::get(wa, 1));
+        f2 s, ds;
+        Act::bwd2(a, &s, &ds);
+        if (Act::near_root(a.x) || Act::near_root(a.y)) {
+            Act::fix_root(a.x, &ds.x);
+            Act::fix_root(a.y, &ds.y);
+        }
+        const f2 c = make_float2(Cd::get(wc, 0), Cd::get(wc, 1));
+        const f2 b = make_float2(Cd::get(wb, 0), Cd::get(wb, 1));
+        const f2 ra = mul2(mul2(c, ds), b);                    // dc * act'(a) * b
+        const f2 rb = mul2(c, s);                              // dc * act(a)
+        da[0] = ra.x;
+        da[1] = ra.y;
+        db[0] = rb.x;
+        db[1] = rb.y;
+    } else {
+        float s, ds;
+        const float a = Cd::get(wa, 0);
+        Act::template bwd_main<Exact>(a, &s, &ds);
+        if (Act::near_root(a)) Act::fix_root(a, &ds);
+        const float c = Cd::get(wc, 0), b = Cd::get(wb, 0);
+        da[0] = c * ds * b;                                    // dc * act'(a) * b
+        db[0] = c * s;                                         // dc * act(a)
     }
 }
 
@@ -260,9 +283,7 @@ __global__ void __launch_bounds__(kThreads) glu_kernel(const Params p)
                     for (int j = 0; j < W; ++j) {
                         float f0[PW], f1[PW];
                         if constexpr (DIR == kFwd) {
-#pragma unroll
-                            for (int e = 0; e < PW; ++e)
-                                f0[e] = op_fwd<Act, kExact>(C::get(va[k][j], e), C::get(vb[k][j], e));
+                            fwd_word<Act, kExact, C>(va[k][j], vb[k][j], f0);
                         } else {
                             bwd_word<Act, kExact, C>(va[k][j], vb[k][j], vc[k][j], f0, f1);
                         }

@@ -31,11 +31,21 @@
 // rounding of the scaled arguments (the tanh polynomial, x^2) would be
 // amplified by up to 2z^2 in the tails, so those arguments are carried as
 // (hi, lo) float pairs and the first-order effect of `lo` is applied
-// analytically.  For fp16/bf16 outputs the plain fp32 forms are far below
-// half an output ulp and the corrections are skipped; there exp(-t) is taken
-// as 2^(-t log2 e) with the hardware base-2 exponential (ex2.approx, relative
-// error ~2^-22, subnormal results kept) and 1/(1+e), whose argument lies in
-// [1, 2], with the hardware reciprocal (rcp.approx, ~1 ulp).
+// analytically.
+//
+// For fp16/bf16 outputs the plain fp32 forms are far below half an output ulp
+// and the corrections are skipped.  That path works on PAIRS of elements (the
+// two halves of a 32-bit storage word) with the packed fp32x2 add, multiply
+// and fused multiply-add of sm_100 and later (one instruction for both
+// elements, IEEE round-to-nearest, subnormals kept), which halves the
+// arithmetic instructions a 16-bit element costs; a single element is the
+// pair (x, x), so the vector body and the scalar row tails give identical
+// bits.  There exp(-t) is the square of 2^(-t log2(e) / 2) from the hardware
+// base-2 exponential with flush-to-zero (ex2.approx.ftz, relative error
+// ~2^-22): the half exponent stays a normal number wherever the result
+// matters, and the square, an IEEE multiply, reaches the subnormal range
+// correctly (silu(-88) in bf16 needs e^-88 = 6e-39).  1/(1+e), whose argument
+// lies in [1, 2], is the hardware reciprocal (rcp.approx, ~1 ulp).
 #pragma once
 #include <cuda_runtime.h>
 #include <math.h>
@@ -49,35 +59,68 @@ struct SigmoidParts {
     float sm;     // 1 - sigmoid(x) = sigmoid(-x), formed without cancellation
 };
 
-// e^(-t) for t >= 0.
+// The scalar forms below serve f32 storage (Exact == true) only.
 template <bool Exact>
-__device__ __forceinline__ float exp_neg(float t)
+__device__ __forceinline__ SigmoidParts sigmoid_parts(float x)
 {
-    if (Exact) return expf(-t);
+    static_assert(Exact, "16-bit storage takes sigmoid_pair");
+    SigmoidParts p;
+    p.e = expf(-fabsf(x));
+    p.r = __frcp_rn(1.0f + p.e);                       // 1 + e in [1, 2]
+    float er = __fmul_rn(p.e, p.r);
+    p.s = x >= 0.0f ? p.r : er;
+    p.sm = x >= 0.0f ? er : p.r;
+    return p;
+}
+
+// ---------------------------------------------------------------- pairs
+// Two fp32 values in one register pair, for the 16-bit storage path.
+
+using f2 = float2;
+__device__ __forceinline__ f2 splat(float v) { return make_float2(v, v); }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ f2 abs2(f2 x) { return make_float2(fabsf(x.x), fabsf(x.y)); }
+
+__device__ __forceinline__ float ex2_ftz(float h)
+{
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(t * -1.44269504f));   // -t log2(e)
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(h));
     return y;
 }
 
-// 1/d for d in [1, 2] (never subnormal, so flush-to-zero cannot change it).
-template <bool Exact>
-__device__ __forceinline__ float recip_1_2(float d)
+__device__ __forceinline__ float rcp_ftz(float d)   // d in [1, 2]: never subnormal
 {
-    if (Exact) return __frcp_rn(d);
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
     return y;
 }
 
-template <bool Exact>
-__device__ __forceinline__ SigmoidParts sigmoid_parts(float x)
+// 2^(2h), h <= 0, as the square of the hardware 2^h: 2^h is normal down to
+// h = -126, so the result is right down to 2^-252 (0 below), subnormals
+// included.
+__device__ __forceinline__ f2 exp2_twice(f2 h)
 {
-    SigmoidParts p;
-    p.e = exp_neg<Exact>(fabsf(x));
-    p.r = recip_1_2<Exact>(1.0f + p.e);
-    float er = __fmul_rn(p.e, p.r);
-    p.s = x >= 0.0f ? p.r : er;
-    p.sm = x >= 0.0f ? er : p.r;
+    const f2 y = make_float2(ex2_ftz(h.x), ex2_ftz(h.y));
+    return mul2(y, y);
+}
+
+constexpr float kNegHalfLog2e = -0.721347520f;      // -log2(e) / 2: e^-t = 2^(2 (t kNegHalfLog2e))
+
+// sigmoid(w) = m r and sigmoid(-w) = m' r for a pair, with e = exp(-|w|),
+// d = 1 + e, r = 1/d, m = 1 (w >= 0) or e (w < 0), m' the other one.
+struct SigmoidPair {
+    f2 e, d, r, m;
+};
+
+__device__ __forceinline__ SigmoidPair sigmoid_pair(f2 w)
+{
+    SigmoidPair p;
+    p.e = exp2_twice(mul2(abs2(w), splat(kNegHalfLog2e)));
+    p.d = add2(p.e, splat(1.0f));
+    p.r = make_float2(rcp_ftz(p.d.x), rcp_ftz(p.d.y));
+    p.m = make_float2(w.x >= 0.0f ? 1.0f : p.e.x, w.y >= 0.0f ? 1.0f : p.e.y);
     return p;
 }
 
@@ -128,15 +171,28 @@ __device__ __forceinline__ bool near_root(float x, const RootSeries r)
 }
 
 // Lower tail of the standard normal:
-//     Phi(-x) = exp(-x^2/2) * t * P(t),  t = 1/(1 + 0.3 x),  x >= 0,
-// with P a polynomial fitted to the exact ratio (Mills' ratio form): degree 7
-// for bf16/f16 storage (relative error of P <= 2.7e-6 in float32), degree 10
-// for f32 storage (<= 1.4e-7).  The coefficients are produced by
-// gen_phi_tail.py next to this file.  The exponential is returned too: it is
-// also sqrt(2 pi) phi(x), the density the GeGLU-erf backward needs.  For f32
-// storage, x^2 is carried as p + pe (exact) and exp(-x^2/2) =
-// exp(-p/2) (1 - pe/2), and 1/(1 + 0.3 x) is rounded correctly.
+//     Phi(-x) = exp(-x^2/2) * t * P(t),  t = 1/(1 + C x),  x >= 0,
+// with P a polynomial fitted to the exact ratio (Mills' ratio form):
+//   - degree 4, C = 0.4, for the forward on bf16/f16 storage (relative error
+//     of P <= 9.5e-5: below a quarter of the f16 half-ulp 2^-12, a twentieth
+//     of the bf16 one);
+//   - degree 7, C = 0.3, for the backward on bf16/f16 storage (<= 2.7e-6:
+//     next to the root of act' the terms Phi and x phi cancel and magnify the
+//     error of Phi up to ~130 times before the root series takes over);
+//   - degree 10, C = 0.3, for f32 storage (<= 1.4e-7).
+// The coefficients are produced by gen_phi_tail.py next to this file.  The
+// exponential is returned too: it is also sqrt(2 pi) phi(x), the density the
+// GeGLU-erf backward needs.  For f32 storage, x^2 is carried as p + pe
+// (exact) and exp(-x^2/2) = exp(-p/2) (1 - pe/2), and 1/(1 + 0.3 x) is
+// rounded correctly.
 constexpr float kPhiTailC = 0.3f;
+constexpr float kPhiTailC4 = 0.4f;
+__host__ __device__ constexpr float phi_tail_coef4(int i)
+{
+    constexpr float p4[5] = {1.595728099e-01f, 1.605101526e-01f, 1.205828786e-01f, 1.440442950e-01f,
+                             -8.475755900e-02f};
+    return p4[i];
+}
 __host__ __device__ constexpr float phi_tail_coef(bool exact, int i)
 {
     constexpr float p7[8] = {1.196823716e-01f, 1.197295263e-01f, 1.077751145e-01f,
@@ -157,22 +213,46 @@ struct PhiTail {
 template <bool Exact>
 __device__ __forceinline__ PhiTail phi_tail(float x)   // x = |a| >= 0
 {
+    static_assert(Exact, "16-bit storage takes phi_tail_pair");
     PhiTail r;
-    float t;
-    if (Exact) {
-        const float xc = fminf(x, 40.0f);                  // Phi(-40) is 0 in fp32
-        const float p = __fmul_rn(xc, xc);
-        r.e = expf(-0.5f * p) * (1.0f - 0.5f * fmaf(xc, xc, -p));
-        t = __frcp_rn(fmaf(kPhiTailC, x, 1.0f));
-    } else {
-        r.e = exp_neg<false>(0.5f * x * x);
-        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(kPhiTailC, x, 1.0f)));   // t in (0, 1]
-    }
-    constexpr int kDeg = Exact ? 10 : 7;
-    float poly = phi_tail_coef(Exact, kDeg);
+    const float xc = fminf(x, 40.0f);                  // Phi(-40) is 0 in fp32
+    const float p = __fmul_rn(xc, xc);
+    r.e = expf(-0.5f * p) * (1.0f - 0.5f * fmaf(xc, xc, -p));
+    const float t = __frcp_rn(fmaf(kPhiTailC, x, 1.0f));
+    constexpr int kDeg = 10;
+    float poly = phi_tail_coef(true, kDeg);
 #pragma unroll
-    for (int i = kDeg - 1; i >= 0; --i) poly = fmaf(poly, t, phi_tail_coef(Exact, i));
+    for (int i = kDeg - 1; i >= 0; --i) poly = fmaf(poly, t, phi_tail_coef(true, i));
     r.q = r.e * (t * poly);
+    return r;
+}
+
+template <int DEG>
+__host__ __device__ constexpr float tail_coef(int i)
+{
+    if constexpr (DEG == 4) return phi_tail_coef4(i);
+    else return phi_tail_coef(false, i);
+}
+
+struct PhiTailPair {
+    f2 q;   // Phi(-x)
+    f2 e;   // exp(-x^2 / 2)
+};
+
+// phi_tail for a pair, 16-bit storage: DEG = 4 (forward) or 7 (backward).
+template <int DEG>
+__device__ __forceinline__ PhiTailPair phi_tail_pair(f2 x)   // x = |a| >= 0
+{
+    static_assert(DEG == 4 || DEG == 7, "fitted degrees");
+    constexpr float C = DEG == 4 ? kPhiTailC4 : kPhiTailC;
+    PhiTailPair r;
+    r.e = exp2_twice(mul2(mul2(x, x), splat(0.5f * kNegHalfLog2e)));   // e^(-x^2/2)
+    const f2 d = fma2(x, splat(C), splat(1.0f));
+    const f2 t = make_float2(rcp_ftz(d.x), rcp_ftz(d.y));                // (0, 1]
+    f2 poly = splat(tail_coef<DEG>(DEG));
+#pragma unroll
+    for (int i = DEG - 1; i >= 0; --i) poly = fma2(poly, t, splat(tail_coef<DEG>(i)));
+    r.q = mul2(r.e, mul2(t, poly));
     return r;
 }
 
@@ -203,29 +283,47 @@ __device__ __forceinline__ float tanh_arg(float x, float *lo)
 // --------------------------------------------------------------------------
 // Each activation: act(x) for the forward, and (act, act') for the backward.
 
+// For 16-bit storage (Exact == false) every activation works on pairs
+// (fwd2, bwd2); its scalar form is the pair (x, x), so that one element gets
+// the same bits wherever it sits.
+
 struct Silu {
+    __device__ __forceinline__ static f2 fwd2(f2 x)
+    {
+        const SigmoidPair p = sigmoid_pair(x);
+        return mul2(x, mul2(p.m, p.r));                     // x sigmoid(x)
+    }
+    // act and act' without the root series (see bwd)
+    __device__ __forceinline__ static void bwd2(f2 x, f2 *act, f2 *dact)
+    {
+        const SigmoidPair p = sigmoid_pair(x);
+        *act = mul2(x, mul2(p.m, p.r));
+        // silu' = ((1+e) m + x e) / (1+e)^2, the numerator as one FMA; its
+        // cancellation near the root is left to the series
+        const f2 num = fma2(x, p.e, mul2(p.d, p.m));
+        *dact = mul2(num, mul2(p.r, p.r));
+    }
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
-        SigmoidParts p = sigmoid_parts<Exact>(x);
+        if (!Exact) return fwd2(splat(x)).x;
+        SigmoidParts p = sigmoid_parts<true>(x);
         return x * p.s;
     }
-    // act and act' without the root series (see bwd)
     template <bool Exact>
     __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
-        SigmoidParts p = sigmoid_parts<Exact>(x);
-        *act = x * p.s;
-        float num;
-        if (Exact) {
-            num = x >= 0.0f ? fmaf(x, p.e, 1.0f + p.e)          // 1 + e + x e
-                            : p.e * ((1.0f + x) + p.e);         // e (1 + x + e)
-        } else {
-            // the same numerator as (1+e) m + x e, m = 1 (x >= 0) or e (x < 0):
-            // one FMA; its cancellation near the root is left to the series
-            const float d = 1.0f + p.e;
-            num = fmaf(x, p.e, d * (x >= 0.0f ? 1.0f : p.e));
+        if (!Exact) {
+            f2 a, d;
+            bwd2(splat(x), &a, &d);
+            *act = a.x;
+            *dact = d.x;
+            return;
         }
+        SigmoidParts p = sigmoid_parts<true>(x);
+        *act = x * p.s;
+        const float num = x >= 0.0f ? fmaf(x, p.e, 1.0f + p.e)      // 1 + e + x e
+                                    : p.e * ((1.0f + x) + p.e);     // e (1 + x + e)
         *dact = num * (p.r * p.r);
     }
     __device__ __forceinline__ static bool near_root(float x) { return glu::near_root(x, silu_root()); }
@@ -239,16 +337,41 @@ struct Silu {
 };
 
 struct GeluErf {
+    __device__ __forceinline__ static f2 cdf2(f2 x, f2 q)     // Phi(x) from q = Phi(-|x|)
+    {
+        const f2 upper = fma2(q, splat(-1.0f), splat(1.0f));  // 1 - q
+        return make_float2(x.x <= 0.0f ? q.x : upper.x, x.y <= 0.0f ? q.y : upper.y);
+    }
+    __device__ __forceinline__ static f2 fwd2(f2 x)
+    {
+        const PhiTailPair t = phi_tail_pair<4>(abs2(x));
+        return mul2(x, cdf2(x, t.q));                           // x Phi(x)
+    }
+    __device__ __forceinline__ static void bwd2(f2 x, f2 *act, f2 *dact)
+    {
+        const PhiTailPair t = phi_tail_pair<7>(abs2(x));
+        const f2 cdf = cdf2(x, t.q);
+        *act = mul2(x, cdf);
+        *dact = fma2(x, mul2(splat(kInvSqrt2Pi), t.e), cdf);   // Phi + x phi
+    }
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
-        const float q = phi_tail<Exact>(fabsf(x)).q;       // Phi(-|x|)
+        if (!Exact) return fwd2(splat(x)).x;
+        const float q = phi_tail<true>(fabsf(x)).q;        // Phi(-|x|)
         return x * (x <= 0.0f ? q : 1.0f - q);              // x Phi(x)
     }
     template <bool Exact>
     __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
-        const PhiTail t = phi_tail<Exact>(fabsf(x));
+        if (!Exact) {
+            f2 a, d;
+            bwd2(splat(x), &a, &d);
+            *act = a.x;
+            *dact = d.x;
+            return;
+        }
+        const PhiTail t = phi_tail<true>(fabsf(x));
         const float cdf = x <= 0.0f ? t.q : 1.0f - t.q;     // Phi(x)
         *act = x * cdf;
         *dact = fmaf(x, kInvSqrt2Pi * t.e, cdf);            // Phi + x phi
@@ -264,14 +387,35 @@ struct GeluErf {
 };
 
 struct GeluTanh {
+    __device__ __forceinline__ static f2 arg2(f2 x)          // w = x (C1 + C3 x^2)
+    {
+        return mul2(x, fma2(splat(kC3Hi), mul2(x, x), splat(kC1Hi)));
+    }
+    __device__ __forceinline__ static f2 fwd2(f2 x)
+    {
+        const SigmoidPair p = sigmoid_pair(arg2(x));
+        return mul2(x, mul2(p.m, p.r));                     // x sigmoid(w)
+    }
+    __device__ __forceinline__ static void bwd2(f2 x, f2 *act, f2 *dact)
+    {
+        const f2 w = arg2(x);
+        const SigmoidPair p = sigmoid_pair(w);
+        const f2 s = mul2(p.m, p.r);                        // sigmoid(w)
+        const f2 sm = mul2(make_float2(w.x >= 0.0f ? p.e.x : 1.0f, w.y >= 0.0f ? p.e.y : 1.0f), p.r);
+        // clamping x leaves act' unchanged (see the scalar form) and finite
+        const f2 xc = make_float2(fminf(fmaxf(x.x, -1.0e4f), 1.0e4f), fminf(fmaxf(x.y, -1.0e4f), 1.0e4f));
+        const f2 dw = fma2(splat(3.0f * kC3Hi), mul2(xc, xc), splat(kC1Hi));
+        *act = mul2(x, s);
+        *dact = mul2(s, fma2(mul2(xc, sm), dw, splat(1.0f)));
+    }
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
+        if (!Exact) return fwd2(splat(x)).x;
         float lo;
-        float w = tanh_arg<Exact>(x, &lo);
-        SigmoidParts p = sigmoid_parts<Exact>(w);
-        float s = p.s;
-        if (Exact) s = fmaf(s * p.sm, lo, s);              // sigmoid(w + lo)
+        float w = tanh_arg<true>(x, &lo);
+        SigmoidParts p = sigmoid_parts<true>(w);
+        const float s = fmaf(p.s * p.sm, lo, p.s);          // sigmoid(w + lo)
         return x * s;
     }
     __device__ __forceinline__ static bool near_root(float x) { return glu::near_root(x, gelu_tanh_root()); }
@@ -285,11 +429,17 @@ struct GeluTanh {
     template <bool Exact>
     __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
+        if (!Exact) {
+            f2 a, d;
+            bwd2(splat(x), &a, &d);
+            *act = a.x;
+            *dact = d.x;
+            return;
+        }
         float lo;
-        float w = tanh_arg<Exact>(x, &lo);
-        SigmoidParts p = sigmoid_parts<Exact>(w);
-        float s = p.s;
-        if (Exact) s = fmaf(s * p.sm, lo, s);
+        float w = tanh_arg<true>(x, &lo);
+        SigmoidParts p = sigmoid_parts<true>(w);
+        const float s = fmaf(p.s * p.sm, lo, p.s);
         // Beyond |x| = 1e4 either 1 - sigmoid(w) or sigmoid(w) is exactly 0, so
         // clamping x inside the bracket leaves act' unchanged and keeps it finite.
         float xc = fminf(fmaxf(x, -1.0e4f), 1.0e4f);
@@ -301,15 +451,23 @@ struct GeluTanh {
 };
 
 struct Relu {
+    __device__ __forceinline__ static float relu(float x) { return x > 0.0f ? x : (x != x ? x : 0.0f); }
+    __device__ __forceinline__ static f2 fwd2(f2 x) { return make_float2(relu(x.x), relu(x.y)); }
+    __device__ __forceinline__ static void bwd2(f2 x, f2 *act, f2 *dact)
+    {
+        *act = fwd2(x);
+        *dact = make_float2(x.x > 0.0f ? 1.0f : (x.x != x.x ? x.x : 0.0f),   // 0 at x == 0
+                            x.y > 0.0f ? 1.0f : (x.y != x.y ? x.y : 0.0f));
+    }
     template <bool Exact>
     __device__ __forceinline__ static float fwd(float x)
     {
-        return x > 0.0f ? x : (x != x ? x : 0.0f);          // NaN propagates
+        return relu(x);                                     // NaN propagates
     }
     template <bool Exact>
     __device__ __forceinline__ static void bwd_main(float x, float *act, float *dact)
     {
-        *act = x > 0.0f ? x : (x != x ? x : 0.0f);
+        *act = relu(x);
         *dact = x > 0.0f ? 1.0f : (x != x ? x : 0.0f);      // 0 at x == 0
     }
     __device__ __forceinline__ static bool near_root(float) { return false; }   // act' has no root
