@@ -594,6 +594,8 @@ CASES = {
     "c4": ("bwd_bf16_outliers", "bwd", "silu", "split", True, "SwiGLU bwd bf16 4096x28672, da->a, db->b"),
     "metric_fwd": ("metric_bf16", "fwd", "silu", "split", False, "SwiGLU fwd bf16 4096x14336"),
     "metric_bwd": ("metric_bf16", "bwd", "silu", "split", False, "SwiGLU bwd bf16 4096x14336"),
+    "metric_step": ("metric_bf16", "step", "silu", "split", False,
+                    "SwiGLU fwd + bwd bf16 4096x14336 (one benchmark step: two launches)"),
 }
 
 
@@ -615,8 +617,15 @@ def run_case(args):
     """One named workload launched --warmup + --steps times, each launch timed
     with CUDA events on its stream; in-place cases restore their inputs before
     every launch, outside the timed pair.  This is the command the per-config
-    ncu captures profile (`-k regex:glu_kernel -s <warmup> -c 1`).  Prints one
-    JSON line (not the benchmark's line)."""
+    ncu captures profile (`-k regex:glu_kernel -s <warmup> -c 1`).
+
+    With --graph N the N launches of one repetition (2 N for metric_step) are
+    captured into a CUDA graph and the graph is replayed --warmup + --steps
+    times: the sustained form, back to back with the launch overlap, that
+    `ncu --graph-profiling graph -s <warmup> -c 1` measures as one workload.
+    In-place cases then run without restores (each launch works on the
+    previous one's output; the arithmetic per element is the same).
+    Prints one JSON line (not the benchmark's line)."""
     import torch
     import glu_activation_mlps_gb300 as glu
 
@@ -628,12 +637,12 @@ def run_case(args):
     E_ = glu_synth.ELEM_BYTES[dt]
     code, a_ = glu.DTYPE[dt], glu.ACT[act]
     dev = torch.device("cuda", 0)
-    sh = torch.cuda.current_stream(dev).cuda_stream
 
     def put(x):
         return torch.from_numpy(x.view(np.int32 if x.dtype == np.uint32 else np.int16)).to(dev)
 
     keep = []          # (live tensor, pristine copy) pairs restored before each launch
+    launches = []      # functions of the stream handle, one kernel launch each
     if layout == "concat":
         X = put(d["x"])
         R, C = X.shape[0], d["n_cols"]
@@ -641,50 +650,72 @@ def run_case(args):
         ys = 2 * C if inplace else C
         if inplace:
             keep.append((X, X.clone()))
-
-        def launch():
-            return L.glu_fwd(X.data_ptr(), 2 * C, None, 0, Y.data_ptr(), ys, R, C, glu.LAYOUT["concat"], a_, code, sh)
+        launches.append(lambda sh: L.glu_fwd(X.data_ptr(), 2 * C, None, 0, Y.data_ptr(), ys, R, C,
+                                             glu.LAYOUT["concat"], a_, code, sh))
     else:
         A, B = put(d["a"]), put(d["b"])
         R, C = A.shape
-        if direction == "fwd":
+        if direction in ("fwd", "step"):
             Y = torch.empty_like(A)
-
-            def launch():
-                return L.glu_fwd(A.data_ptr(), C, B.data_ptr(), C, Y.data_ptr(), C, R, C, 0, a_, code, sh)
-        else:
+            launches.append(lambda sh: L.glu_fwd(A.data_ptr(), C, B.data_ptr(), C, Y.data_ptr(), C, R, C, 0, a_,
+                                                 code, sh))
+        if direction in ("bwd", "step"):
             DC = put(d["dc"])
             DA, DB = (A, B) if inplace else (torch.empty_like(A), torch.empty_like(B))
             if inplace:
                 keep += [(A, A.clone()), (B, B.clone())]
-
-            def launch():
-                return L.glu_bwd(DC.data_ptr(), C, A.data_ptr(), C, B.data_ptr(), C, DA.data_ptr(), C,
-                                 DB.data_ptr(), C, R, C, 0, a_, code, sh)
+            launches.append(lambda sh: L.glu_bwd(DC.data_ptr(), C, A.data_ptr(), C, B.data_ptr(), C, DA.data_ptr(),
+                                                 C, DB.data_ptr(), C, R, C, 0, a_, code, sh))
     del d
+    per_unit = {"fwd": 3, "bwd": 5, "step": 8}[direction]
+    nbytes = per_unit * E_ * R * C
+
+    def run_once(sh):
+        for fn in launches:
+            st = fn(sh)
+            if st:
+                raise glu.GluError(st, "case launch")
+
     stream = torch.cuda.current_stream(dev)
+    graph = None
+    reps = 1
+    if args.graph:
+        reps = args.graph
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            run_once(side.cuda_stream)           # once outside the capture
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(reps):
+                run_once(side.cuda_stream)
+        torch.cuda.synchronize()
     times = []
     info = None
     for k in range(args.warmup + args.steps):
-        for live, pristine in keep:
-            live.copy_(pristine)
+        if graph is None:
+            for live, pristine in keep:
+                live.copy_(pristine)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        st = launch()
+        if graph is None:
+            run_once(stream.cuda_stream)
+            info = dict(glu.glu_last_launch())
+        else:
+            graph.replay()
         e1.record(stream)
-        if st:
-            raise glu.GluError(st, "case launch")
-        info = dict(glu.glu_last_launch())
         if k >= args.warmup:
             times.append((e0, e1))
     torch.cuda.synchronize()
-    us = [a.elapsed_time(b) * 1e3 for a, b in times]
-    nbytes = (3 if direction == "fwd" else 5) * E_ * R * C
+    us = [a.elapsed_time(b) * 1e3 / reps for a, b in times]
     peak, src = measured_peak()
     med = statistics.median(us)
     print(json.dumps({"case": args.case, "what": desc, "rows": R, "cols": C, "dtype": dt, "act": act,
                       "dir": direction, "in_place": inplace, "algorithmic_bytes": nbytes,
-                      "launches": args.warmup + args.steps, "timed": len(us),
+                      "graph_reps": reps if graph is not None else None,
+                      "launches": (args.warmup + args.steps) * reps * len(launches), "timed": len(us),
                       "us_median": round(med, 3), "us_min": round(min(us), 3),
                       "gbs": round(nbytes / med / 1e3, 1), "frac_of_copy": round(nbytes / med / 1e3 / peak, 4),
                       "peak_source": src, "launch": info}), flush=True)
@@ -975,23 +1006,48 @@ def oracle_rows(orc, d, r0, r1, threads):
     orc.bwd_threaded("silu", "bf16", dc, a, b, threads)
 
 
+def oracle_gbs(orc, d, threads, budget_s):
+    """The oracle's throughput (forward + backward, algorithmic bytes over
+    wall time) on `threads` host threads.  One untimed call first (thread
+    start-up, first touch of the outputs, clock ramp), then a call on 16 rows
+    sizes the blocks so that one call takes about a quarter of `budget_s`;
+    blocks of consecutive rows are timed until `budget_s` has passed.
+    Returns (GB/s, rows timed, seconds timed, rows per call)."""
+    oracle_rows(orc, d, 0, 16, threads)
+    t = time.perf_counter()
+    oracle_rows(orc, d, 0, 16, threads)
+    per_row = (time.perf_counter() - t) / 16
+    block = int(max(16, min(ROWS, budget_s / 4 / max(per_row, 1e-9))))
+    spent, done, r0 = 0.0, 0, 0
+    while spent < budget_s:
+        if r0 + block > ROWS:
+            r0 = 0
+        s = time.perf_counter()
+        oracle_rows(orc, d, r0, r0 + block, threads)
+        spent += time.perf_counter() - s
+        done += block
+        r0 += block
+    return done * COLS * 8 * E / spent / 1e9, done, spent, block
+
+
 def cpu_baseline(d, budget_s=3.0):
-    """The oracle, as it stands, on the host cores: consecutive 128-row blocks
-    of the workload until `budget_s` of wall time has passed (or all rows)."""
+    """The oracle, as it stands, on the host cores: all of them (the reported
+    value) and one, each timed for about `budget_s` seconds after a warm-up
+    call (oracle_gbs)."""
     import oracle as orc
     orc.build()
     threads = os.cpu_count() or 1
-    t0 = time.perf_counter()
-    rows = 0
-    while rows < ROWS and (time.perf_counter() - t0) < budget_s:
-        r1 = min(ROWS, rows + 128)
-        oracle_rows(orc, d, rows, r1, threads)
-        rows = r1
-    dt = time.perf_counter() - t0
-    nbytes = rows * COLS * 8 * E
-    return {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"rows 0..{rows} of the 4096x14336 bf16 workload (fwd + bwd, "
-                      f"{rows * COLS} elements, {dt:.2f} s wall on {threads} threads)"}
+    gbs, rows, secs, block = oracle_gbs(orc, d, threads, budget_s)
+    gbs1, rows1, secs1, block1 = oracle_gbs(orc, d, 1, budget_s)
+
+    def sample(r, sec, blk, th):
+        return (f"{r} rows of the 4096x14336 bf16 workload in blocks of {blk} rows (fwd + bwd, "
+                f"{r * COLS} elements, {sec:.2f} s on {th} thread{'s' if th > 1 else ''}, after one "
+                f"untimed call)")
+    return {"value": round(gbs, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": sample(rows, secs, block, threads),
+            "all_cores": {"value": round(gbs, 3), "cores": threads},
+            "single_thread": {"value": round(gbs1, 3), "cores": 1, "sample": sample(rows1, secs1, block1, 1)}}
 
 
 def run_reference(args):
@@ -1017,13 +1073,18 @@ def run_reference(args):
     nbytes = rows * COLS * 8 * E
     value = args.steps * nbytes / total / 1e9
     sample = f"rows 0..{rows} of the 4096x14336 bf16 workload per step (fwd + bwd, {rows * COLS} elements)"
+    # beside it, the same oracle on one thread (a short bounded sample)
+    gbs1, rows1, secs1, block1 = oracle_gbs(orc, d, 1, min(10.0, args.ref_seconds / 6))
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config({"parallelism": f"{threads} host threads", "math": "f64"}),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "all_cores": {"value": round(value, 3), "cores": threads},
+                         "single_thread": {"value": round(gbs1, 3), "cores": 1,
+                                           "sample": f"{rows1} rows in blocks of {block1} rows, {secs1:.2f} s "
+                                                     "on 1 thread, after one untimed call"}},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -1052,6 +1113,8 @@ def main():
                     help="launch one named workload (" + ", ".join(CASES) + ", or sweep:<act>:<dtype>:<dir>:<H>) "
                          "--warmup + --steps times and print its per-launch time (the command the per-config "
                          "ncu captures profile)")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="--case: capture N repetitions of the case into one CUDA graph and time its replays")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -39,13 +39,22 @@ std::atomic<void *> g_scratch_addr[kMaxDevices];
 std::mutex g_setup_mutex;
 
 // Device address of g_noalloc_scratch on the current device, looked up on the
-// first call made on that device.
-int scratch_address(void **out)
+// first call made on that device (devices numbered kMaxDevices and above are
+// looked up on every call).  *dev_out receives the device number.
+int scratch_address(void **out, int *dev_out)
 {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return glu::cuda_fail(e);
-    if (dev < 0 || dev >= kMaxDevices) return GLU_ERR_CUDA;
+    *dev_out = dev;
+    if (dev < 0) return glu::cuda_fail(cudaErrorInvalidDevice);
+    if (dev >= kMaxDevices) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return glu::cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        *out = p;
+        return GLU_OK;
+    }
     void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
     if (!p) {
         std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -58,6 +67,14 @@ int scratch_address(void **out)
     }
     *out = p;
     return GLU_OK;
+}
+
+// A failed copy may mean the cached address is stale (the device was reset,
+// which reloads the library's module): the next call looks it up again.
+int forget_address(int dev, cudaError_t e)
+{
+    if (dev >= 0 && dev < kMaxDevices) g_scratch_addr[dev].store(nullptr, std::memory_order_release);
+    return glu::cuda_fail(e);
 }
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -104,7 +121,8 @@ extern "C" int glu_fwd_host_noalloc(const void *a, int64_t a_stride, const void 
     if (block > n_rows) block = n_rows;
 
     void *base = nullptr;
-    if (int st = scratch_address(&base)) return st;
+    int dev = -1;
+    if (int st = scratch_address(&base, &dev)) return st;
     char *d_in[2], *d_out;
     {
         char *p = static_cast<char *>(base);
@@ -122,7 +140,7 @@ extern "C" int glu_fwd_host_noalloc(const void *a, int64_t a_stride, const void 
         const int64_t rows = n_rows - r0 < block ? n_rows - r0 : block;
         for (int m = 0; m < n_in; ++m) {
             cudaError_t e = stage_rows(d_in[m], h_in[m], h_stride[m], in_width, r0, rows, E, true, s);
-            if (e != cudaSuccess) return glu::cuda_fail(e);
+            if (e != cudaSuccess) return forget_address(dev, e);
         }
         const int st = concat ? glu_fwd(d_in[0], 2 * n_cols, nullptr, 0, d_out, n_cols, rows, n_cols, layout,
                                         act, dtype, stream)
@@ -130,7 +148,7 @@ extern "C" int glu_fwd_host_noalloc(const void *a, int64_t a_stride, const void 
                                         act, dtype, stream);
         if (st != GLU_OK) return st;
         cudaError_t e = stage_rows(d_out, c.y0, c.sy0, n_cols, r0, rows, E, false, s);
-        if (e != cudaSuccess) return glu::cuda_fail(e);
+        if (e != cudaSuccess) return forget_address(dev, e);
     }
     return GLU_OK;
 }

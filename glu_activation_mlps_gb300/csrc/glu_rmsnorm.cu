@@ -958,6 +958,27 @@ BwdFn pick_narrow(int dtype, bool dh)
     }
 }
 
+// Blocks of the narrow kernel resident on one SM at once (the occupancy
+// query, asked once per device, dtype and dh variant; devices numbered 64
+// and above are asked on every call).
+cudaError_t narrow_resident(int dev, int dtype, bool dh, int *out)
+{
+    static std::atomic<int> cache[64][6];
+    const int key = (dtype == GLU_F32 ? 0 : dtype == GLU_F16 ? 1 : 2) * 2 + (dh ? 1 : 0);
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev][key].load(std::memory_order_relaxed);
+        if (c > 0) { *out = c; return cudaSuccess; }
+    }
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, reinterpret_cast<const void *>(pick_narrow(dtype, dh)), kRmsBwdNarrowThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev][key].store(n, std::memory_order_relaxed);
+    *out = n;
+    return cudaSuccess;
+}
+
 BwdFn pick_bwd(int dtype, int nv, bool dh, bool prod)
 {
     switch (dtype) {
@@ -1148,13 +1169,22 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
     }
     // Rows of up to 128 vectors take the non-persistent narrow kernel instead
     // (4 rows per team, one access per operand per thread) when its grid fits
-    // on the GPU at once (two blocks per SM): every block adds to dgamma, and
-    // more blocks than that queue their additions on the same addresses
-    // (measured: 262144 rows of 64 took 2.5 times the persistent kernel's time).
+    // on the GPU at once (the blocks resident per SM, as the occupancy query
+    // reports them, times the SMs): every block adds to dgamma, and more blocks
+    // than that queue their additions on the same addresses (measured: 262144
+    // rows of 64 took 2.5 times the persistent kernel's time).
     const int64_t narrow_tpr = ((n_cols + V - 1) / V + 31) / 32 * 32;
     const int64_t narrow_rows = kRmsBwdNarrowThreads / narrow_tpr * kRmsBwdNarrowRows;
-    const bool narrow = staged && n_cols <= int64_t(128) * V &&
-                        (n_rows + narrow_rows - 1) / narrow_rows <= 2 * int64_t(sms);
+    bool narrow = staged && n_cols <= int64_t(128) * V;
+    if (narrow) {
+        int resident = 0;
+        e = narrow_resident(dev, dtype, dh != nullptr, &resident);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return glu::cuda_fail(e);
+        }
+        narrow = (n_rows + narrow_rows - 1) / narrow_rows <= int64_t(resident) * sms;
+    }
     const bool prod = staged && !narrow && n_cols <= int64_t(1024) * V;
     const int nv = !staged ? 0 : n_cols <= int64_t(256) * V ? 1 : n_cols <= int64_t(512) * V ? 2 : 4;
     const int ept = staged ? nv * V : 16;

@@ -211,6 +211,9 @@ int glu_bwd_host(const void *dc, int64_t dc_stride,
  *     GLU_ERR_WORKSPACE.
  *   - The first call on each device looks up the array's device address (a
  *     CUDA runtime query); make that first call before any stream capture.
+ *     A device reset (cudaDeviceReset) reloads the library's module and may
+ *     move the array: the address kept from before is then stale.  A call
+ *     whose copy fails forgets it, so the next call looks it up again.
  *   - Every call uses the same array, which keeps the last call's contents
  *     (no part of it needs to start at zero): calls whose work can overlap on
  *     the GPU race on it, so order them, e.g. on one stream.
