@@ -864,6 +864,110 @@ def run_gemm(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- the whole gated MLP
+
+def run_mlp(args):
+    """glu_mlp_fwd on one decoder layer's MLP (4096 tokens, hidden 4096,
+    intermediate 14336, bf16, SwiGLU): the gate/up GEMM with the activation in
+    its epilogue, then the down GEMM, in row chunks whose y stays in L2.
+    Against the unfused path (cuBLAS GEMM into [gate | up], glu_fwd, cuBLAS
+    down GEMM) and against glu_gemm_fwd + glu_gemm_nt over all rows at once (y
+    through HBM), all in one process.  Prints one JSON line."""
+    import torch
+    import glu_activation_mlps_gb300 as glu
+
+    glu.build()
+    L = glu.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev).manual_seed(9)
+    M, H, I = GM, GK, GI
+    x = torch.randn(M, H, device=dev, generator=gen).to(torch.bfloat16)
+    w = (torch.randn(2 * I, H, device=dev, generator=gen) / H ** 0.5).to(torch.bfloat16)
+    wg, wu = w[:I], w[I:]
+    wd = (torch.randn(H, I, device=dev, generator=gen) / I ** 0.5).to(torch.bfloat16)
+    out = torch.empty(M, H, device=dev, dtype=torch.bfloat16)
+    y = torch.empty(M, I, device=dev, dtype=torch.bfloat16)
+    h = torch.empty(M, 2 * I, device=dev, dtype=torch.bfloat16)
+    ws_bytes = L.glu_mlp_workspace_bytes(M, I, 2)
+    ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    flops = 2 * M * H * 2 * I + 2 * M * I * H
+
+    def fused():
+        st = L.glu_mlp_fwd(x.data_ptr(), H, wg.data_ptr(), wu.data_ptr(), H, wd.data_ptr(), I, out.data_ptr(), H,
+                           M, H, I, 0, 2, ws.data_ptr(), ws_bytes, s)
+        if st:
+            raise glu.GluError(st, "glu_mlp_fwd")
+
+    def whole():
+        st = L.glu_gemm_fwd(x.data_ptr(), H, wg.data_ptr(), wu.data_ptr(), H, y.data_ptr(), I, M, H, I, 0, 2, s)
+        if st:
+            raise glu.GluError(st, "glu_gemm_fwd")
+        st = L.glu_gemm_nt(y.data_ptr(), I, wd.data_ptr(), I, out.data_ptr(), H, M, I, H, 2, s)
+        if st:
+            raise glu.GluError(st, "glu_gemm_nt")
+
+    def unfused():
+        torch.matmul(x, w.T, out=h)
+        st = L.glu_fwd(h.data_ptr(), 2 * I, None, 0, y.data_ptr(), I, M, I, 1, 0, 2, s)
+        if st:
+            raise glu.GluError(st, "glu_fwd")
+        torch.matmul(y, wd.T, out=out)
+
+    def timed(fn, K, W, clocks=None):
+        for _ in range(W):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark(True)
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if clocks:
+            clocks.mark(False)
+        return e0.elapsed_time(e1) / K
+
+    K, W = max(1, args.steps), max(3, args.warmup)
+    clocks = ClockSampler(gpu_selector(0))
+    clocks.start()
+    fused_ms = timed(fused, K, W, clocks)
+    clock_info = clocks.stop()
+    whole_ms = timed(whole, K, W)
+    unfused_ms = timed(unfused, K, W)
+    down_ms = timed(lambda: torch.matmul(y, wd.T, out=out), K, W)
+    nt_ms = timed(lambda: L.glu_gemm_nt(y.data_ptr(), I, wd.data_ptr(), I, out.data_ptr(), H, M, I, H, 2, s), K, W)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    peak = float(peaks["bf16_tflops"])
+    tf = flops / (fused_ms * 1e-3) / 1e12
+    down_flops = 2 * M * I * H
+    line = {
+        "metric": "gated MLP (gate/up GEMM + SwiGLU + down GEMM), TFLOP/s (bf16, M=4096 H=4096 I=14336)",
+        "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": round(fused_ms, 5), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "one decoder layer's MLP: x 4096x4096, w_gate and w_up 14336x4096, w_down "
+                               "4096x14336 (N(0,1), N(0,1/4096), N(0,1/14336), bf16)",
+                   "chunk_rows": ws_bytes // (2 * ((I + 7) // 8 * 8)), "workspace_bytes": ws_bytes},
+        "roofline": {"bound": "tensor", "kernel": "glu_mlp_fwd", "achieved": round(tf, 1), "peak": peak,
+                     "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)",
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None, "algorithmic_flops": flops},
+        "comparison": {"fused_ms": round(fused_ms, 4),
+                       "glu_gemm_fwd_then_glu_gemm_nt_all_rows_ms": round(whole_ms, 4),
+                       "cublas_gemm_glu_fwd_cublas_gemm_ms": round(unfused_ms, 4),
+                       "speedup_vs_unfused": round(unfused_ms / fused_ms, 4),
+                       "glu_gemm_nt_down_ms": round(nt_ms, 4), "cublas_down_ms": round(down_ms, 4),
+                       "glu_gemm_nt_vs_cublas": round(down_ms / nt_ms, 4),
+                       "glu_gemm_nt_tflops": round(down_flops / (nt_ms * 1e-3) / 1e12, 1)},
+        "gpu_launches": K * 2 * -(-M // (ws_bytes // (2 * ((I + 7) // 8 * 8)))),
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- residual add + RMSNorm
 
 def run_rmsnorm(args):
@@ -975,7 +1079,7 @@ def run_rmsnorm(args):
     main = case(4096, 4096, clocks)
     clock_info = clocks.stop()
     sweep = [case(4096, H) for H in (1024, 2048, 8192, 16384)]
-    bwd = [backward(4096, H) for H in (1024, 4096, 16384)]
+    bwd = [backward(4096, H) for H in (512, 1024, 2048, 4096, 8192, 16384)]
     line = {
         "metric": "fused residual add + RMSNorm achieved HBM GB/s (bf16, 4096 tokens x hidden 4096)",
         "value": main["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
@@ -1102,6 +1206,8 @@ def main():
                     help="time glu_gemm_fwd on one MLP layer against cuBLAS + glu_fwd (one JSON line)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="--gemm: skip the other layer shapes")
+    ap.add_argument("--mlp", action="store_true",
+                    help="time glu_mlp_fwd on one decoder layer's MLP against cuBLAS + glu_fwd + cuBLAS")
     ap.add_argument("--rmsnorm", action="store_true",
                     help="time glu_add_rmsnorm_fwd on one decoder block against torch's add + rms_norm")
     ap.add_argument("--table", action="store_true",
@@ -1128,6 +1234,9 @@ def main():
 
     if args.gemm:
         run_gemm(args)
+        return
+    if args.mlp:
+        run_mlp(args)
         return
     if args.rmsnorm:
         run_rmsnorm(args)

@@ -33,6 +33,7 @@ EXPORTS = ("glu_fwd", "glu_bwd", "glu_fwd_host", "glu_bwd_host", "glu_fwd_host_n
            "glu_host_workspace_bytes",
            "glu_status_string", "glu_last_cuda_error", "glu_version", "glu_last_launch",
            "glu_set_tuning", "glu_get_tuning", "glu_wait_timeouts", "glu_wait_selftest", "glu_gemm_fwd",
+           "glu_gemm_nt", "glu_mlp_fwd", "glu_mlp_workspace_bytes",
            "glu_add_rmsnorm_fwd", "glu_add_rmsnorm_bwd")
 
 
@@ -111,6 +112,12 @@ def lib() -> ctypes.CDLL:
             L.glu_wait_selftest.restype = ci
             L.glu_gemm_fwd.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, i64, ci, ci, vp]
             L.glu_gemm_fwd.restype = ci
+            L.glu_gemm_nt.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, ci, vp]
+            L.glu_gemm_nt.restype = ci
+            L.glu_mlp_fwd.argtypes = [vp, i64, vp, vp, i64, vp, i64, vp, i64, i64, i64, i64, ci, ci, vp, sz, vp]
+            L.glu_mlp_fwd.restype = ci
+            L.glu_mlp_workspace_bytes.argtypes = [i64, i64, ci]
+            L.glu_mlp_workspace_bytes.restype = sz
             L.glu_add_rmsnorm_fwd.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i64, vp, i64, i64,
                                               ctypes.c_float, ci, vp]
             L.glu_add_rmsnorm_fwd.restype = ci
@@ -205,6 +212,20 @@ def glu_wait_selftest(stream=None) -> None:
 
 def glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream) -> int:
     return lib().glu_gemm_fwd(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream)
+
+
+def glu_gemm_nt(a, a_stride, b, b_stride, d, d_stride, M, K, N, dtype, stream) -> int:
+    return lib().glu_gemm_nt(a, a_stride, b, b_stride, d, d_stride, M, K, N, dtype, stream)
+
+
+def glu_mlp_fwd(x, x_stride, w_gate, w_up, w_stride, w_down, w_down_stride, out, out_stride, M, H, I, act, dtype,
+                workspace, workspace_bytes, stream) -> int:
+    return lib().glu_mlp_fwd(x, x_stride, w_gate, w_up, w_stride, w_down, w_down_stride, out, out_stride, M, H, I,
+                             act, dtype, workspace, workspace_bytes, stream)
+
+
+def glu_mlp_workspace_bytes(M, I, dtype) -> int:
+    return lib().glu_mlp_workspace_bytes(M, I, dtype)
 
 
 def glu_add_rmsnorm_fwd(x, x_stride, residual, res_stride, gamma, h, h_stride, y, y_stride, rstd,
@@ -366,6 +387,61 @@ def gemm_fwd(x, w_gate, w_up, *, y=None, act: str = "silu", stream=None):
     if st:
         raise GluError(st, "glu_gemm_fwd")
     return y
+
+
+def gemm_nt(a, b, *, d=None, stream=None):
+    """d = a @ b^T on the tensor cores (the MLP's down projection).  a is
+    (..., K); b is (N, K) in the nn.Linear layout; f16 or bf16."""
+    import torch
+    n_rows, a_stride = _rows(a, "a")
+    if b.dim() != 2 or b.shape[1] != a.shape[-1] or b.dtype != a.dtype:
+        raise ValueError("b must be (N, K) with K = a.shape[-1] and a's dtype")
+    _, b_stride = _rows(b, "b")
+    N, K = b.shape
+    if d is None:
+        d = torch.empty((*a.shape[:-1], N), dtype=a.dtype, device=a.device)
+    if tuple(d.shape) != (*a.shape[:-1], N) or d.dtype != a.dtype:
+        raise ValueError("d has the wrong shape or dtype")
+    _, d_stride = _rows(d, "d")
+    st = glu_gemm_nt(a.data_ptr(), a_stride, b.data_ptr(), b_stride, d.data_ptr(), d_stride, n_rows, K, N,
+                     _dtype_code(a), _stream(stream))
+    if st:
+        raise GluError(st, "glu_gemm_nt")
+    return d
+
+
+def mlp_fwd(x, w_gate, w_up, w_down, *, out=None, act: str = "silu", workspace=None, stream=None):
+    """out = (act(x @ w_gate^T) * (x @ w_up^T)) @ w_down^T; x is (..., H), the
+    gate and up weights (I, H), the down weights (H, I).  The workspace (a
+    uint8 device tensor) is allocated here when not given."""
+    import torch
+    n_rows, x_stride = _rows(x, "x")
+    H = x.shape[-1]
+    if w_gate.dim() != 2 or w_up.shape != w_gate.shape or w_gate.shape[1] != H:
+        raise ValueError("w_gate and w_up must both be (I, H)")
+    I = w_gate.shape[0]
+    if tuple(w_down.shape) != (H, I):
+        raise ValueError("w_down must be (H, I)")
+    if any(w.dtype != x.dtype for w in (w_gate, w_up, w_down)):
+        raise ValueError("x and the weights must have one dtype")
+    _, wg_stride = _rows(w_gate, "w_gate")
+    _, wu_stride = _rows(w_up, "w_up")
+    if wg_stride != wu_stride:
+        raise ValueError("w_gate and w_up must have one row stride")
+    _, wd_stride = _rows(w_down, "w_down")
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    _, out_stride = _rows(out, "out")
+    code = _dtype_code(x)
+    if workspace is None:
+        workspace = torch.empty(max(16, glu_mlp_workspace_bytes(max(n_rows, 1), max(I, 1), code)),
+                                dtype=torch.uint8, device=x.device)
+    st = glu_mlp_fwd(x.data_ptr(), x_stride, w_gate.data_ptr(), w_up.data_ptr(), wg_stride, w_down.data_ptr(),
+                     wd_stride, out.data_ptr(), out_stride, n_rows, H, I, ACT[act], code, workspace.data_ptr(),
+                     workspace.numel(), _stream(stream))
+    if st:
+        raise GluError(st, "glu_mlp_fwd")
+    return out
 
 
 def add_rmsnorm(x, residual, gamma, eps: float = 1e-5, *, h=None, y=None, rstd=None, stream=None):

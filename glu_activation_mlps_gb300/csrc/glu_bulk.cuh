@@ -134,12 +134,8 @@ __global__ void __launch_bounds__(BulkShape<DIR, NARROW>::kThreads, NARROW ? 2 :
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float f0[PW], f1[PW];
-#pragma unroll
-                for (int e = 0; e < PW; ++e) {
-                    const float a = C::get(wa[j], e), b = C::get(wb[j], e);
-                    if constexpr (DIR == kFwd) f0[e] = op_fwd<Act, kExact>(a, b);
-                    else op_bwd<Act, kExact>(C::get(wc[j], e), a, b, f0[e], f1[e]);
-                }
+                if constexpr (DIR == kFwd) fwd_word<Act, kExact, C>(wa[j], wb[j], f0);
+                else bwd_word<Act, kExact, C>(wa[j], wb[j], wc[j], f0, f1);
                 o0[j] = C::put(f0);
                 if constexpr (DIR == kBwd) o1[j] = C::put(f1);
             }

@@ -296,6 +296,40 @@ __device__ __forceinline__ void tile_origin(const Params &p, int t, int &mb, int
     ib = r / gsize;
 }
 
+// The plain product D = A B^T (the down projection of an MLP) runs on the same
+// kernel with PlainGemm in place of the activation: a tile is 2 BN output
+// columns, the two weight slots hold consecutive BN-row slices of the one B
+// matrix, and the epilogue only rounds the fp32 sums.
+struct PlainGemm {};
+
+// 32 fp32 accumulator columns of one row rounded once and packed two per word.
+template <class Cd>
+__device__ __forceinline__ void plain_pack(const uint32_t (&g)[32], uint32_t (&packed)[16])
+{
+    static_assert(Cd::kPerWord == 2, "16-bit outputs");
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float f[2] = {__uint_as_float(g[j]), __uint_as_float(g[j + 1])};
+        packed[j / 2] = Cd::put(f);
+    }
+}
+
+// y = act(g) * u for 32 accumulator columns of one row, two at a time (the
+// pair forms of the 16-bit path), rounded once and packed two per word.
+template <class Act, class Cd>
+__device__ __forceinline__ void epilogue_pack(const uint32_t (&g)[32], const uint32_t (&u)[32], uint32_t (&packed)[16])
+{
+    static_assert(Cd::kPerWord == 2, "16-bit outputs");
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const f2 gg = make_float2(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
+        const f2 uu = make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1]));
+        const f2 y = mul2(Act::fwd2(gg), uu);
+        const float f[2] = {y.x, y.y};
+        packed[j / 2] = Cd::put(f);
+    }
+}
+
 template <class Act, class T, int BN, int CTAS>
 __global__ void __launch_bounds__(kThreads, 1)
     glu_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
@@ -305,6 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using S = Shape<BN, CTAS>;
     using Cd = Codec<T>;
     constexpr int ST = S::kStages;
+    constexpr bool kPlain = std::is_same<Act, PlainGemm>::value;
+    constexpr int kOutCols = kPlain ? 2 * BN : BN;      // output columns of one tile
     constexpr uint32_t kIdesc = idesc_f16(std::is_same<T, __nv_bfloat16>::value ? 1 : 0, S::kMmaM, S::kMmaN);
 
     extern __shared__ unsigned char smem_raw[];
@@ -369,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = cluster; t < n_tiles && !*abort_flag; t += n_clusters) {
                 int mb, ib;
                 tile_origin(p, t, mb, ib);
-                const int m0 = mb * S::kMmaM + int(rank) * BM, i0 = ib * BN;
+                const int m0 = mb * S::kMmaM + int(rank) * BM, i0 = ib * kOutCols;
+                const int i1 = kPlain ? i0 + BN : i0;          // rows of the second weight slot
                 for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
                     const uint32_t s = it % ST, use = it / ST;
                     if (*abort_flag) break;
@@ -383,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         arrive_expect_tx_local(bar, p.a_bytes + uint32_t(2 * S::kTileB));
                         tma_load<1>(st, &tm_x, kt * BK, m0, bar);
                         tma_load<1>(st + S::kTileA, &tm_wg, kt * BK, i0, bar);
-                        tma_load<1>(st + S::kTileA + S::kTileB, &tm_wu, kt * BK, i0, bar);
+                        tma_load<1>(st + S::kTileA + S::kTileB, &tm_wu, kt * BK, i1, bar);
                     } else {
                         // both blocks' copies count on block 0's barrier, which
                         // alone arrives, expecting the bytes of the pair (block
@@ -395,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else
                             bar = mapa(bar, 0);
                         tma_load<2>(st, &tm_x, kt * BK, m0, bar);
-                        tma_load<2>(st + S::kTileA, rank == 0 ? &tm_wg : &tm_wu, kt * BK, i0, bar);
+                        tma_load<2>(st + S::kTileA, rank == 0 ? &tm_wg : &tm_wu, kt * BK, rank == 0 ? i0 : i1, bar);
                     }
                 }
             }
@@ -471,15 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, ib;
             tile_origin(p, t, mb, ib);
             const int m = mb * S::kMmaM + int(rank) * BM + q * 32 + lane;
-            const int i0 = ib * BN;
+            const int i0 = ib * kOutCols;
             const uint32_t acc = tmem + lane_base + uint32_t(ab * S::kAccCols);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < kOutCols; c0 += 32) {
                 uint32_t g[32], u[32];
                 tmem_ld32(acc + uint32_t(c0), g);
-                tmem_ld32(acc + uint32_t(BN + c0), u);
+                if constexpr (!kPlain) tmem_ld32(acc + uint32_t(BN + c0), u);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (c0 + 32 == BN) {          // all of this tile read: hand the accumulator back
+                if (c0 + 32 == kOutCols) {    // all of this tile read: hand the accumulator back
                     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
@@ -489,16 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             arrive_cluster(mapa(saddr(&acc_empty[ab]), 0));
                     }
                 }
+                uint32_t packed[16];
+                if constexpr (kPlain)
+                    plain_pack<Cd>(g, packed);
+                else
+                    epilogue_pack<Act, Cd>(g, u, packed);
                 if (p.tma_store) {
-                    uint32_t packed[32 / Cd::kPerWord];
-#pragma unroll
-                    for (int j = 0; j < 32; j += Cd::kPerWord) {
-                        float f[Cd::kPerWord];
-#pragma unroll
-                        for (int e = 0; e < Cd::kPerWord; ++e)
-                            f[e] = op_fwd<Act, false>(__uint_as_float(g[j + e]), __uint_as_float(u[j + e]));
-                        packed[j / Cd::kPerWord] = Cd::put(f);
-                    }
                     // this warp's 32 rows x 32 columns: row `lane` is 64 bytes,
                     // its 16-byte chunk c stored at chunk c ^ ((lane / 2) % 4)
                     const uint32_t buf = saddr(ystage) + uint32_t(q * 2 + (n_boxes & 1)) * (kYBox * kYBox * 2);
@@ -517,15 +550,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 if (m >= p.M) continue;
-                uint32_t packed[32 / Cd::kPerWord];
-#pragma unroll
-                for (int j = 0; j < 32; j += Cd::kPerWord) {
-                    float f[Cd::kPerWord];
-#pragma unroll
-                    for (int e = 0; e < Cd::kPerWord; ++e)
-                        f[e] = op_fwd<Act, false>(__uint_as_float(g[j + e]), __uint_as_float(u[j + e]));
-                    packed[j / Cd::kPerWord] = Cd::put(f);
-                }
                 const int i = i0 + c0;
                 char *dst = p.y + int64_t(m) * p.y_stride + int64_t(i) * int64_t(sizeof(T));
                 if (p.vec_store && i + 32 <= p.I) {
@@ -610,6 +634,7 @@ bool make_map(CUtensorMap *m, bool bf16, const void *base, int64_t rows, int64_t
 }
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
+constexpr int kPlainAct = 4;        // the kernel table's index of the plain product
 
 template <class T, int BN, int CTAS>
 KernelFn pick_act(int act)
@@ -619,6 +644,7 @@ KernelFn pick_act(int act)
     case 1: return glu_gemm_kernel<GeluErf, T, BN, CTAS>;
     case 2: return glu_gemm_kernel<GeluTanh, T, BN, CTAS>;
     case 3: return glu_gemm_kernel<Relu, T, BN, CTAS>;
+    case 4: return glu_gemm_kernel<PlainGemm, T, BN, CTAS>;     // D = A B^T
     default: return nullptr;
     }
 }
@@ -654,13 +680,13 @@ Variant pick(bool bf16, int act, int bn, int ctas)
 // and I = 14336, M <= 128 gets 96 (150 tiles in one round, fewer weight rows
 // per block than 128); M = 8192 gets 128 where a rule on columns alone picked
 // 64 for 1 % less wave quantisation and ran 1.8 times slower.
-int pick_bn(int64_t m_blocks, int64_t I, int64_t slots, int64_t a_rows)
+int pick_bn(int64_t m_blocks, int64_t I, int64_t slots, int64_t a_rows, int cols_per_bn = 1)
 {
-    if (I <= 64) return 64;
+    if (I <= 64 * cols_per_bn) return 64;
     int best = 128;
     int64_t best_cost = -1;
     for (int bn : {128, 96, 64}) {
-        const int64_t tiles = m_blocks * ((I + bn - 1) / bn);
+        const int64_t tiles = m_blocks * ((I + cols_per_bn * bn - 1) / (cols_per_bn * bn));
         const int64_t cost = (tiles + slots - 1) / slots * (a_rows + 2 * bn);
         if (best_cost < 0 || cost < best_cost) {
             best = bn;
@@ -673,7 +699,7 @@ int pick_bn(int64_t m_blocks, int64_t I, int64_t slots, int64_t a_rows)
 // Per kernel variant and device: the shared-memory opt-in done, and how many
 // blocks (one shape) or pairs (the other) fit on the GPU at once.
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_slots[kMaxDevices][2][4][6];
+std::atomic<int> g_slots[kMaxDevices][2][5][6];     // [device][bf16][activation, 4 = plain][variant]
 
 bool overlap(uintptr_t a0, uint64_t alen, uintptr_t b0, uint64_t blen)
 {
@@ -695,12 +721,17 @@ cudaError_t timeouts(unsigned int *count, bool reset)
 }  // namespace gemm
 }  // namespace glu
 
-extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate, const void *w_up,
-                            int64_t w_stride, void *y, int64_t y_stride, int64_t M, int64_t K, int64_t I,
-                            glu_act_t act, glu_dtype_t dtype, glu_stream_t stream)
+namespace glu {
+namespace gemm {
+namespace {
+
+// glu_gemm_fwd (act 0..3: y = act(x w_gate^T) * (x w_up^T), I output columns)
+// and glu_gemm_nt (act 4: y = x w^T with w_gate = w_up = w, I = its rows).
+int run_gemm(const void *x, int64_t x_stride, const void *w_gate, const void *w_up, int64_t w_stride, void *y,
+             int64_t y_stride, int64_t M, int64_t K, int64_t I, int act, glu_dtype_t dtype, glu_stream_t stream)
 {
-    using namespace glu::gemm;
-    if (act < GLU_ACT_SILU || act > GLU_ACT_RELU || (dtype != GLU_F16 && dtype != GLU_BF16)) return GLU_ERR_ENUM;
+    const bool plain = act == kPlainAct;
+    if (act < GLU_ACT_SILU || act > kPlainAct || (dtype != GLU_F16 && dtype != GLU_BF16)) return GLU_ERR_ENUM;
     if (M < 0 || K < 0 || I < 0 || M > INT32_MAX || K > INT32_MAX || I > INT32_MAX) return GLU_ERR_SHAPE;
     if (M == 0 || I == 0) {
         glu::record_launch(glu_launch_info_t{});
@@ -743,7 +774,7 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     if (e != cudaSuccess) { (void)cudaGetLastError(); return glu::cuda_fail(e); }
     const int64_t rows_per_block = int64_t(BM) * ctas;
     const int64_t tile_rows = ctas == 1 ? (M + 7) / 8 * 8 : rows_per_block;     // rows of x a tile loads
-    const int bn = pick_bn((M + rows_per_block - 1) / rows_per_block, I, sms / ctas, tile_rows);
+    const int bn = pick_bn((M + rows_per_block - 1) / rows_per_block, I, sms / ctas, tile_rows, plain ? 2 : 1);
     const Variant v = pick(bf16, act, bn, ctas);
 
     cudaLaunchConfig_t cfg{};
@@ -806,7 +837,7 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     p.K = int(K);
     p.k_tiles = int((K + BK - 1) / BK);
     p.m_blocks = int((M + rows_per_block - 1) / rows_per_block);
-    p.i_blocks = int((I + bn - 1) / bn);
+    p.i_blocks = int((I + (plain ? 2 : 1) * bn - 1) / ((plain ? 2 : 1) * bn));
     // row blocks per group: their x rows (about 48 MiB at most) stay in L2
     // while the weight slices stream past them once
     const int64_t block_bytes = rows_per_block * K * E;
@@ -838,8 +869,130 @@ extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate,
     info.unroll = ctas;
     info.threads = kThreads;
     info.grid = int32_t(clusters * ctas);
-    info.path = 3;
+    info.path = plain ? 5 : 3;
     info.vector_units = tiles;
     glu::record_launch(info);
+    return GLU_OK;
+}
+
+}  // namespace
+}  // namespace gemm
+}  // namespace glu
+
+extern "C" int glu_gemm_fwd(const void *x, int64_t x_stride, const void *w_gate, const void *w_up,
+                            int64_t w_stride, void *y, int64_t y_stride, int64_t M, int64_t K, int64_t I,
+                            glu_act_t act, glu_dtype_t dtype, glu_stream_t stream)
+{
+    if (act < GLU_ACT_SILU || act > GLU_ACT_RELU) return GLU_ERR_ENUM;
+    return glu::gemm::run_gemm(x, x_stride, w_gate, w_up, w_stride, y, y_stride, M, K, I, act, dtype, stream);
+}
+
+extern "C" int glu_gemm_nt(const void *a, int64_t a_stride, const void *b, int64_t b_stride, void *d,
+                           int64_t d_stride, int64_t M, int64_t K, int64_t N, glu_dtype_t dtype, glu_stream_t stream)
+{
+    return glu::gemm::run_gemm(a, a_stride, b, b, b_stride, d, d_stride, M, K, N, glu::gemm::kPlainAct, dtype,
+                               stream);
+}
+
+// ---------------------------------------------------------------- the gated MLP
+
+namespace glu {
+namespace gemm {
+namespace {
+
+// The rows run in chunks of at most this many bytes of y.  Measured on GB300
+// (4096 x 4096 x 14336, bf16): chunks of 1536 rows, whose 44 MiB of y stay in
+// L2 between the two products, took 0.847 ms; the whole batch in one chunk,
+// y through HBM, 0.778 ms: launches of fewer rows lose more to tile rounds and
+// pipeline fill than the 2 x 117 MB of y traffic cost.  So a chunk is as large
+// as the workspace allows, and the default workspace holds the whole y up to
+// this cap.
+constexpr uint64_t kMlpChunkBytes = uint64_t(1) << 30;
+
+int64_t round_up8(int64_t v) { return (v + 7) / 8 * 8; }
+
+// Rows of y a chunk holds within `bytes`: whole 256-row blocks of the pair
+// shape when more than 256 rows fit, else as many rows as fit; at most M.
+int64_t mlp_chunk_rows(int64_t M, int64_t I, uint64_t bytes)
+{
+    const uint64_t row = uint64_t(round_up8(I)) * 2;
+    int64_t rows = int64_t(bytes / row);
+    if (rows > 256) rows = rows / 256 * 256;
+    return rows < M ? rows : M;
+}
+
+}  // namespace
+}  // namespace gemm
+}  // namespace glu
+
+extern "C" size_t glu_mlp_workspace_bytes(int64_t M, int64_t I, glu_dtype_t dtype)
+{
+    using namespace glu::gemm;
+    if (M <= 0 || I <= 0 || I > INT32_MAX || (dtype != GLU_F16 && dtype != GLU_BF16)) return 0;
+    return size_t(mlp_chunk_rows(M, I, kMlpChunkBytes)) * size_t(round_up8(I)) * 2;
+}
+
+extern "C" int glu_mlp_fwd(const void *x, int64_t x_stride, const void *w_gate, const void *w_up, int64_t w_stride,
+                           const void *w_down, int64_t w_down_stride, void *out, int64_t out_stride, int64_t M,
+                           int64_t H, int64_t I, glu_act_t act, glu_dtype_t dtype, void *workspace,
+                           size_t workspace_bytes, glu_stream_t stream)
+{
+    using namespace glu::gemm;
+    if (act < GLU_ACT_SILU || act > GLU_ACT_RELU || (dtype != GLU_F16 && dtype != GLU_BF16)) return GLU_ERR_ENUM;
+    if (M < 0 || H < 0 || I < 0 || M > INT32_MAX || H > INT32_MAX || I > INT32_MAX) return GLU_ERR_SHAPE;
+    if (M == 0 || H == 0) {
+        glu::record_launch(glu_launch_info_t{});
+        return GLU_OK;
+    }
+    if (!out || !x || !w_gate || !w_up || (I > 0 && !w_down)) return GLU_ERR_NULL;
+    if (x_stride < H || w_stride < H || out_stride < H || (I > 0 && w_down_stride < I)) return GLU_ERR_STRIDE;
+    const int E = 2;
+    const int64_t ys = round_up8(I);            // the chunk's y rows, 16-byte multiples for the copy engine
+    if (I > 0) {
+        if (!workspace || workspace_bytes < uint64_t(ys) * E) return GLU_ERR_WORKSPACE;
+        // every operand goes through the tensor-memory accelerator: 16-byte
+        // aligned bases and row strides, device memory, checked before the
+        // first launch
+        if (uintptr_t(workspace) % 16 || uintptr_t(x) % 16 || uintptr_t(w_gate) % 16 || uintptr_t(w_up) % 16 ||
+            uintptr_t(w_down) % 16 || (x_stride * E) % 16 || (w_stride * E) % 16 || (w_down_stride * E) % 16)
+            return GLU_ERR_STRIDE;
+    }
+    // out is written while x is still being read (by later chunks): no overlap
+    // with any operand or the workspace
+    const uint64_t olen = (uint64_t(M - 1) * uint64_t(out_stride) + uint64_t(H)) * E;
+    const uint64_t xlen = (uint64_t(M - 1) * uint64_t(x_stride) + uint64_t(H)) * E;
+    const uint64_t wlen = I > 0 ? (uint64_t(I - 1) * uint64_t(w_stride) + uint64_t(H)) * E : 0;
+    const uint64_t dlen = I > 0 ? (uint64_t(H - 1) * uint64_t(w_down_stride) + uint64_t(I)) * E : 0;
+    if (overlap(uintptr_t(out), olen, uintptr_t(x), xlen) || overlap(uintptr_t(out), olen, uintptr_t(w_gate), wlen) ||
+        overlap(uintptr_t(out), olen, uintptr_t(w_up), wlen) || overlap(uintptr_t(out), olen, uintptr_t(w_down), dlen) ||
+        (I > 0 && overlap(uintptr_t(out), olen, uintptr_t(workspace), workspace_bytes)))
+        return GLU_ERR_ALIAS;
+    if (I > 0) {
+        for (const void *q : {x, w_gate, w_up, w_down, static_cast<const void *>(workspace),
+                              static_cast<const void *>(out)}) {
+            bool dev_mem = false;
+            const cudaError_t pe = glu::on_device(q, &dev_mem);
+            if (pe != cudaSuccess) return glu::cuda_fail(pe);
+            if (!dev_mem) return GLU_ERR_VALUE;
+        }
+    }
+    if (I == 0) {           // empty inner sums: out = 0
+        cudaError_t e = cudaMemset2DAsync(out, size_t(out_stride) * E, 0, size_t(H) * E, size_t(M),
+                                          reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return glu::cuda_fail(e);
+        glu::record_launch(glu_launch_info_t{});
+        return GLU_OK;
+    }
+    const uint64_t budget = workspace_bytes < kMlpChunkBytes ? workspace_bytes : kMlpChunkBytes;
+    const int64_t chunk = mlp_chunk_rows(M, I, budget);
+    for (int64_t r0 = 0; r0 < M; r0 += chunk) {
+        const int64_t rows = M - r0 < chunk ? M - r0 : chunk;
+        const char *xr = static_cast<const char *>(x) + r0 * x_stride * E;
+        char *outr = static_cast<char *>(out) + r0 * out_stride * E;
+        int st = glu_gemm_fwd(xr, x_stride, w_gate, w_up, w_stride, workspace, ys, rows, H, I, act, dtype, stream);
+        if (st != GLU_OK) return st;
+        st = glu_gemm_nt(workspace, ys, w_down, w_down_stride, outr, out_stride, rows, I, H, dtype, stream);
+        if (st != GLU_OK) return st;
+    }
     return GLU_OK;
 }

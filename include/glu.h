@@ -25,8 +25,9 @@
  *     stream) and the call returns before it runs.  Pinned host memory
  *     (cudaHostAlloc, cudaHostRegister) is device memory in this sense: the
  *     kernels then read and write it in place over the host link (zero-copy),
- *     except glu_gemm_fwd's operands and glu_add_rmsnorm_bwd's dgamma, which
- *     must be in device memory.
+ *     except the operands of the tensor-core entry points (glu_gemm_fwd,
+ *     glu_gemm_nt, glu_mlp_fwd) and glu_add_rmsnorm_bwd's dgamma, which must
+ *     be in device memory.
  *   - Matrices are row-major with a contiguous last dimension: element (r, c)
  *     of operand X is at X + r * X_stride + c.  Strides are in ELEMENTS of
  *     `dtype`, not bytes, and are ignored when n_rows == 1.
@@ -44,7 +45,7 @@
  *   - Pointers and strides that are 32- or 16-byte aligned use 256- or 128-bit
  *     memory accesses; any other alignment is valid and uses element-wide
  *     accesses.  Alignment is never an error, except for the operands that
- *     glu_gemm_fwd reads through the tensor-memory accelerator.
+ *     the tensor-core entry points read through the tensor-memory accelerator.
  *   - Non-finite inputs are outside the numerical contract; they do not fault.
  */
 #ifndef GLU_H
@@ -100,10 +101,10 @@ typedef enum {
     GLU_ERR_ALIAS = -4,   /* outputs overlap inputs other than exactly, or each other */
     GLU_ERR_ENUM = -5,    /* unknown act, layout or dtype */
     GLU_ERR_CUDA = -6,    /* the CUDA runtime refused a launch or copy; see glu_last_cuda_error() */
-    GLU_ERR_WORKSPACE = -7, /* host-memory entry points: workspace NULL or too small for one row */
+    GLU_ERR_WORKSPACE = -7, /* host-memory entry points, glu_mlp_fwd: workspace NULL or too small for one row */
     GLU_ERR_VALUE = -8      /* an argument out of range: glu_add_rmsnorm_fwd's eps, or an
-                               operand of glu_gemm_fwd or glu_add_rmsnorm_bwd's dgamma
-                               that is not in device memory */
+                               operand of a tensor-core entry point or glu_add_rmsnorm_bwd's
+                               dgamma that is not in device memory */
 } glu_status_t;
 
 /*
@@ -353,6 +354,77 @@ int glu_gemm_fwd(const void *x, int64_t x_stride,
                  void *y, int64_t y_stride,
                  int64_t M, int64_t K, int64_t I,
                  glu_act_t act, glu_dtype_t dtype, glu_stream_t stream);
+
+/*
+ * The plain product on the same tensor-core kernel, the down projection of
+ * the MLP ("Fused Kernels", section 4, "The fused MLP": the gated tile times
+ * the down weights; "Skill: Write a Triton SiLU-Mul (SwiGLU) Kernel",
+ * Purpose: down_proj of the gated product):
+ *
+ *     d[m, n] = round(sum_k a[m, k] * b[n, k]),
+ *
+ * sums in fp32 in the hardware's order, one rounding to nearest-even.
+ *   a, a_stride        M x K (row-major, a_stride >= K).
+ *   b, b_stride        N x K, row n holding output feature n (the nn.Linear
+ *                      layout), b_stride >= K.
+ *   d, d_stride        M x N output, d_stride >= N; no overlap with a or b
+ *                      (GLU_ERR_ALIAS).
+ *   dtype              GLU_F16 or GLU_BF16.
+ * Alignment, device-memory, empty-size, K == 0 (d = 0) and timeout rules as
+ * glu_gemm_fwd.  glu_last_launch reports path = 5.
+ */
+int glu_gemm_nt(const void *a, int64_t a_stride,
+                const void *b, int64_t b_stride,
+                void *d, int64_t d_stride,
+                int64_t M, int64_t K, int64_t N,
+                glu_dtype_t dtype, glu_stream_t stream);
+
+/*
+ * The gated MLP, out = down_proj(act(gate_proj(x)) * up_proj(x)) ("Skill:
+ * Write a Triton SiLU-Mul (SwiGLU) Kernel", Purpose; "Fused Kernels", section
+ * 4, "The fused MLP"):
+ *
+ *     y[m, i]   = round(act(x[m] . w_gate[i]) * (x[m] . w_up[i]))   (glu_gemm_fwd)
+ *     out[m, h] = round(y[m] . w_down[h])                           (glu_gemm_nt)
+ *
+ * y, rounded once to the dtype as glu_gemm_fwd stores it, goes through the
+ * caller's workspace: the rows run in chunks whose y fits it (at most 1 GiB
+ * of y per chunk), two launches per chunk.  Keeping y in registers or tensor
+ * memory instead, as the page's kernel does, would recompute the gate and up
+ * products once per output column tile (16 times at H = 4096); chunks small
+ * enough for y to stay in L2 between the products were measured slower on
+ * GB300 than whole-batch launches (0.847 against 0.778 ms at 4096 x 4096 x
+ * 14336 bf16): smaller launches lose more to tile rounds than the y traffic
+ * costs.
+ *   x, x_stride        M x H activations, x_stride >= H.
+ *   w_gate, w_up       I x H, row stride w_stride >= H.
+ *   w_down             H x I (row h holds output feature h), w_down_stride >= I.
+ *   out, out_stride    M x H output, out_stride >= H; no overlap with any
+ *                      operand or the workspace (GLU_ERR_ALIAS).
+ *   workspace          device memory for one chunk's y, 16-byte aligned:
+ *                      glu_mlp_workspace_bytes(M, I, dtype) bytes, or less
+ *                      (smaller chunks), but at least one row of
+ *                      round_up(I, 8) elements, else GLU_ERR_WORKSPACE.  It
+ *                      holds the last chunk's y on return.
+ * x, the weights, the workspace and out must be device memory (GLU_ERR_VALUE)
+ * with 16-byte aligned bases and strides that are multiples of 8 elements
+ * (GLU_ERR_STRIDE); both are checked before the first launch.  M == 0 or
+ * H == 0: no work; I == 0: out = 0.  Two launches per chunk on `stream`;
+ * glu_last_launch describes the last.  Returns GLU_OK or a negative
+ * glu_status_t.
+ */
+int glu_mlp_fwd(const void *x, int64_t x_stride,
+                const void *w_gate, const void *w_up, int64_t w_stride,
+                const void *w_down, int64_t w_down_stride,
+                void *out, int64_t out_stride,
+                int64_t M, int64_t H, int64_t I,
+                glu_act_t act, glu_dtype_t dtype,
+                void *workspace, size_t workspace_bytes, glu_stream_t stream);
+
+/* Workspace bytes for glu_mlp_fwd to run M rows of intermediate size I in
+ * one chunk (the y of all rows, rows of round_up(I, 8) elements), capped at
+ * 1 GiB (chunks of whole 256-row blocks); 0 for invalid arguments. */
+size_t glu_mlp_workspace_bytes(int64_t M, int64_t I, glu_dtype_t dtype);
 
 /*
  * Fused residual add + RMSNorm ("Skill: Write a Triton Fused Add+RMSNorm

@@ -66,6 +66,8 @@ def lib():
             L.oracle_decode_vec.argtypes = [ci, vp, dp, i64]
             L.oracle_gemm_glu_at.argtypes = [ci, ci, vp, i64, vp, vp, i64, i64, vp, vp, i64, vp, dp, dp, dp, dp]
             L.oracle_gemm_glu_at.restype = None
+            L.oracle_matmul_nt_at.argtypes = [ci, vp, i64, vp, i64, i64, vp, vp, i64, vp, dp, dp]
+            L.oracle_matmul_nt_at.restype = None
             L.oracle_add_rmsnorm.argtypes = [ci, vp, vp, vp, vp, vp, dp, dp, i64, i64, ctypes.c_double]
             L.oracle_add_rmsnorm.restype = None
             L.oracle_add_rmsnorm_bwd.argtypes = [ci, vp, vp, vp, vp, vp, vp, dp, dp, i64, i64]
@@ -262,6 +264,35 @@ def gemm_glu(act_name: str, dtype: str, x, w_gate, w_up):
     mm, ii = np.meshgrid(np.arange(M), np.arange(I), indexing="ij")
     y, *_ = gemm_glu_at(act_name, dtype, x, w_gate, w_up, mm.ravel(), ii.ravel())
     return y.reshape(M, I)
+
+
+def matmul_nt_at(dtype: str, a, b, ms, ns):
+    """d[m, n] = round(a[m] . b[n]) at the listed (m, n) pairs, with the exact
+    (double) sums and the sums of |products|.  a is M x K, b is N x K (bit
+    arrays, row-major, contiguous)."""
+    a, b = _bits(a, dtype), _bits(b, dtype)
+    if a.shape[1] != b.shape[1]:
+        raise ValueError("a is M x K and b is N x K")
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    n = ms.size
+    d = np.empty(n, dtype=BITS_DTYPE[dtype])
+    ex, sa = np.empty(n), np.empty(n)
+    lib().oracle_matmul_nt_at(DTYPES[dtype], _ptr(a), a.shape[1], _ptr(b), b.shape[1], a.shape[1],
+                              _ptr(ms), _ptr(ns), n, _ptr(d), _ptr(ex), _ptr(sa))
+    return d, ex, sa
+
+
+def mlp(act_name: str, dtype: str, x, w_gate, w_up, w_down):
+    """The gated MLP, every output: y = round(act(x w_gate^T) * (x w_up^T)),
+    the intermediate stored in the dtype, then out = round(y w_down^T), with
+    the exact (double) down sums and their sums of |products| (small problems
+    only).  w_down is H x I (row h holds output feature h)."""
+    y = gemm_glu(act_name, dtype, x, w_gate, w_up)
+    M, H = y.shape[0], np.asarray(w_down).shape[0]
+    mm, hh = np.meshgrid(np.arange(M), np.arange(H), indexing="ij")
+    d, ex, sa = matmul_nt_at(dtype, y, w_down, mm.ravel(), hh.ravel())
+    return d.reshape(M, H), y, ex.reshape(M, H), sa.reshape(M, H)
 
 
 # ---- fused residual add + RMSNorm --------------------------------------------

@@ -350,6 +350,31 @@ void oracle_gemm_glu_at(int act, int dtype, const void *x, int64_t sx, const voi
     }
 }
 
+/* The MLP's second half, the down projection ("Skill: Write a Triton SiLU-Mul
+ * (SwiGLU) Kernel", Purpose: down_proj of the gated product; "Fused Kernels",
+ * section 4, "The fused MLP": the gated tile multiplied by the down weights):
+ *   d[m,n] = round(sum_k a[m,k] * b[n,k])
+ * a is M x K (the stored y of the first half), b is N x K (row n holds output
+ * feature n), row strides in elements.  The sum in double, k in order, and
+ * one rounding; the sum of |products| is returned too (it bounds the error of
+ * any reordered fp32 summation).  exact and sabs may be NULL. */
+void oracle_matmul_nt_at(int dtype, const void *a, int64_t sa, const void *b, int64_t sb, int64_t K,
+                         const int64_t *ms, const int64_t *ns, int64_t n, void *d, double *exact, double *sabs)
+{
+    for (int64_t j = 0; j < n; ++j) {
+        double sum = 0.0, tot = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double pv = oracle_decode(load_bits(a, ms[j] * sa + k, dtype), dtype) *
+                              oracle_decode(load_bits(b, ns[j] * sb + k, dtype), dtype);
+            sum += pv;
+            tot += fabs(pv);
+        }
+        store_bits(d, j, dtype, oracle_encode(sum, dtype));
+        if (exact) exact[j] = sum;
+        if (sabs) sabs[j] = tot;
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* Fused residual add + RMSNorm ("Skill: Write a Triton Fused Add+RMSNorm
  * Kernel": Purpose, y = rmsnorm(x + residual) with x + residual written back;

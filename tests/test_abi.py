@@ -17,7 +17,7 @@ import glu_activation_mlps_gb300 as glu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "glu.h")
 
-OK, NULL, SHAPE, STRIDE, ALIAS, ENUM, CUDA = 0, -1, -2, -3, -4, -5, -6
+OK, NULL, SHAPE, STRIDE, ALIAS, ENUM, CUDA, WORKSPACE = 0, -1, -2, -3, -4, -5, -6, -7
 SPLIT, CONCAT = 0, 1
 SILU, RELU = 0, 3
 F32, F16, BF16 = 0, 1, 2
@@ -273,6 +273,56 @@ def test_gemm_valid_call_reaches_the_cuda_runtime_without_a_gpu():
     assert gemm(y=BASE + (3 << 20) + 2, sy=101) == CUDA
     assert gemm(wu=BASE + (1 << 20)) == CUDA
     assert glu.glu_last_cuda_error()
+
+
+# ---- glu_gemm_nt and glu_mlp_fwd -------------------------------------------
+
+def gemm_nt(a=BASE, sa=64, b=BASE + (1 << 20), sb=64, d=BASE + (3 << 20), sd=96, M=4, K=64, N=96, dtype=BF16):
+    return glu.glu_gemm_nt(a, sa, b, sb, d, sd, M, K, N, dtype, None)
+
+
+@cpu_only
+def test_gemm_nt_validation():
+    assert gemm_nt(dtype=F32) == ENUM and gemm_nt(M=-1) == SHAPE and gemm_nt(N=1 << 31) == SHAPE
+    assert gemm_nt(a=None, d=None, M=0) == OK and gemm_nt(b=None, N=0, d=None) == OK
+    assert gemm_nt(a=None) == NULL and gemm_nt(b=None) == NULL and gemm_nt(d=None) == NULL
+    assert gemm_nt(sa=63) == STRIDE and gemm_nt(sb=60) == STRIDE and gemm_nt(sd=95) == STRIDE
+    assert gemm_nt(a=BASE + 2) == STRIDE and gemm_nt(sb=66) == STRIDE
+    assert gemm_nt(d=BASE + 2) == ALIAS and gemm_nt(d=BASE + (1 << 20) - 4) == ALIAS
+    assert gemm_nt(d=BASE + (3 << 20) + 2, sd=101) == CUDA          # valid: reaches the runtime
+
+
+WS = BASE + (6 << 20)
+
+
+def mlp(x=BASE, sx=64, wg=BASE + (1 << 20), wu=BASE + (2 << 20), sw=64, wd=BASE + (4 << 20), sd=96,
+        out=BASE + (3 << 20), so=64, M=4, H=64, I=96, act=SILU, dtype=BF16, ws=WS, ws_bytes=1 << 20):
+    return glu.glu_mlp_fwd(x, sx, wg, wu, sw, wd, sd, out, so, M, H, I, act, dtype, ws, ws_bytes, None)
+
+
+@cpu_only
+def test_mlp_validation():
+    assert mlp(act=4) == ENUM and mlp(dtype=F32) == ENUM
+    assert mlp(M=-1) == SHAPE and mlp(I=-1) == SHAPE and mlp(H=1 << 31) == SHAPE
+    assert mlp(x=None, out=None, M=0) == OK and mlp(x=None, out=None, H=0) == OK
+    assert mlp(x=None) == NULL and mlp(wd=None) == NULL and mlp(out=None) == NULL
+    assert mlp(sx=63) == STRIDE and mlp(sw=63) == STRIDE and mlp(so=60) == STRIDE and mlp(sd=95) == STRIDE
+    # the workspace holds at least one row of y (I rounded up to 8 elements)
+    assert mlp(ws=None) == WORKSPACE and mlp(ws_bytes=2 * 96 - 2) == WORKSPACE
+    assert mlp(I=97, sd=104, ws_bytes=2 * 97) == WORKSPACE and mlp(I=97, sd=104, ws_bytes=2 * 104) == CUDA
+    # the tensor-memory accelerator's alignment rules, before any launch
+    assert mlp(ws=WS + 8) == STRIDE and mlp(wd=BASE + (4 << 20) + 2) == STRIDE and mlp(sd=100) == STRIDE
+    # out may overlap nothing: not x, a weight or the workspace
+    assert mlp(out=BASE) == ALIAS and mlp(out=BASE + (4 << 20) + 64) == ALIAS and mlp(out=WS + 512) == ALIAS
+    assert mlp() == CUDA and glu.glu_last_cuda_error()              # valid: reaches the runtime
+
+
+def test_mlp_workspace_bytes():
+    ws = glu.glu_mlp_workspace_bytes
+    assert ws(4096, 14336, BF16) == 4096 * 14336 * 2          # the whole y
+    assert ws(65536, 14336, BF16) == 37376 * 14336 * 2        # 1 GiB holds 37449 rows: 146 blocks of 256
+    assert ws(100, 14336, BF16) == 100 * 14336 * 2 and ws(10, 97, F16) == 10 * 104 * 2
+    assert ws(0, 64, BF16) == 0 and ws(4, 64, F32) == 0 and ws(4, 0, BF16) == 0
 
 
 # ---- glu_add_rmsnorm_fwd -----------------------------------------------------

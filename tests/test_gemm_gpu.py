@@ -92,10 +92,12 @@ def check_bound(orc, act, dt, y_bits, g, u, sg, su, K, what):
 # column tiles are 64, 96 or 128 wide (the rule in expected_tiles), and the
 # shapes below take each width in both block shapes: one block 96 at
 # (5, 520, 14336) and 128 at (100, 64, 38912); pairs 96 at (256, 64, 14336)
-# and 128 at (1024, 16, 14336); 64 elsewhere.
+# and 128 at (700, 16, 14336) and (1024, 16, 14336); 64 elsewhere.  A ragged
+# last row block whose second block reads no row at all (1100, 72, 300), and
+# ragged rows and columns (2047, 136, 520).
 SHAPES = [(1, 8, 1), (128, 64, 128), (127, 72, 65), (300, 200, 300), (129, 1000, 40), (257, 328, 200),
           (64, 4096, 64), (700, 256, 520), (333, 136, 100), (5, 520, 14336), (256, 64, 14336),
-          (100, 64, 38912), (1024, 16, 14336)]
+          (100, 64, 38912), (700, 16, 14336), (1024, 16, 14336), (1100, 72, 300), (2047, 136, 520)]
 
 
 def cluster_size(M, I):

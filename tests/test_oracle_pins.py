@@ -514,6 +514,57 @@ def test_gemm_glu_exact_integer_case(orc):
     assert orc.decode("bf16", y2)[0, 0] == orc.round_to("bf16", orc.act("gelu_tanh", [4.0]) * 4.0)[0]
 
 
+# --------------------------------------------------------------------------- the MLP's down projection
+# "Fused Kernels", section 4, "The fused MLP"; the product y @ w_down^T.
+
+def test_matmul_nt_matches_numpy(orc):
+    """d = a b^T against numpy's float64 matmul of the decoded operands, both
+    the exact sum and its one rounding, at scattered (m, n) pairs; operand
+    order matters (b a^T differs)."""
+    rng = np.random.default_rng(41)
+    M, N, K = 9, 13, 300
+    for dt in ("bf16", "f16"):
+        a = glu_synth.normal_bits(rng, (M, K), 1.0, dt)
+        b = glu_synth.normal_bits(rng, (N, K), 1.0, dt)
+        A, B = orc.decode(dt, a), orc.decode(dt, b)
+        ref = A @ B.T
+        ms, ns = rng.integers(0, M, 40), rng.integers(0, N, 40)
+        d, ex, sa = orc.matmul_nt_at(dt, a, b, ms, ns)
+        want = ref[ms, ns]
+        assert np.all(np.abs(ex - want) <= 1e-13 * (np.abs(A[ms]) @ np.abs(B).T)[np.arange(40), ns])
+        assert np.allclose(sa, (np.abs(A[ms]) * np.abs(B[ns])).sum(1), rtol=1e-14, atol=0)
+        assert np.array_equal(d, orc.encode(dt, ex))
+        # the transposed order reads other rows: different values where the shapes allow
+        d2, ex2, _ = orc.matmul_nt_at(dt, b[:M], a[:M], ms % M, ns % M)
+        assert not np.allclose(ex2, ex)
+
+
+def test_matmul_nt_integer_closed_form(orc):
+    """a[m, k] = m + 1, b[n, k] = k - n: d[m, n] = (m + 1) (K (K - 1) / 2 - n K), exact."""
+    M, N, K = 3, 4, 16
+    a = orc.encode("bf16", np.repeat(np.arange(1, M + 1, dtype=float)[:, None], K, 1))
+    b = orc.encode("bf16", np.arange(K, dtype=float)[None, :] - np.arange(N, dtype=float)[:, None])
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    d, ex, _ = orc.matmul_nt_at("bf16", a, b, mm.ravel(), nn.ravel())
+    want = (mm.ravel() + 1) * (K * (K - 1) / 2 - nn.ravel() * K)
+    assert np.array_equal(ex, want) and np.array_equal(orc.decode("bf16", d), want)
+
+
+def test_mlp_is_the_two_products(orc):
+    """mlp() = the gated first half rounded to the dtype, then the down
+    projection of that stored y (numpy's matmul of the decoded y)."""
+    rng = np.random.default_rng(42)
+    M, Hd, I = 6, 40, 24
+    x = glu_synth.normal_bits(rng, (M, Hd), 1.0, "bf16")
+    wg, wu = (glu_synth.normal_bits(rng, (I, Hd), 0.2, "bf16") for _ in range(2))
+    wd = glu_synth.normal_bits(rng, (Hd, I), 0.2, "bf16")
+    out, y, ex, sa = orc.mlp("silu", "bf16", x, wg, wu, wd)
+    assert np.array_equal(y, orc.gemm_glu("silu", "bf16", x, wg, wu))
+    ref = orc.decode("bf16", y) @ orc.decode("bf16", wd).T
+    assert np.allclose(ex, ref, rtol=0, atol=1e-13 * sa.max())
+    assert np.array_equal(out, orc.encode("bf16", ex))
+
+
 # --------------------------------------------------------------------------- residual add + RMSNorm
 # Page: "Skill: Write a Triton Fused Add+RMSNorm Kernel" (AR).
 
