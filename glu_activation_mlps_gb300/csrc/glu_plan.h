@@ -21,7 +21,7 @@ struct Params {
     uint32_t div_magic;           // unit -> (row, unit-in-row) by multiply-shift
     uint32_t div_shift;
     int32_t wide;                 // units >= 2^32: plain 64-bit division
-    int32_t pad;
+    int32_t prefetch;             // ask L2 for the first tile's inputs before waiting on the previous grid
     int64_t rem;                  // tail elements per row (n_cols - vpr * elems-per-unit)
     int64_t tail_units;           // rows * rem
     int64_t tail_col_bytes;       // byte offset of the first tail element in a row
