@@ -273,7 +273,9 @@ def test_back_to_back_dependent_kernels(orc, dependent):
     ReLU, so every product is exact: the GPU chain must equal the oracle's
     chain bit for bit, and any launch that read its input before the previous
     kernel finished writing it would show up as a mismatch.  Run with and
-    without programmatic dependent launch."""
+    without programmatic dependent launch.  The launches (34-50 MB of inputs)
+    also prefetch their first tile into L2 before waiting on the previous
+    launch, which this chain checks cannot expose data older than its writes."""
     glu.glu_set_tuning(0, 0, 0, dependent)
     try:
         rows, cols, dt = 2048, 4096, "bf16"
