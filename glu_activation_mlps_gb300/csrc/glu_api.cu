@@ -33,17 +33,19 @@ constexpr int32_t kDefaultCtasPerSm = -1;     // one block per tile
 // by [dtype][activation][direction], from a sweep on GB300 of 4096 x {4096,
 // 16384} matrices launched back to back: the forward of the heavier GELUs wants
 // two 32-byte accesses in flight (more arithmetic to hide), the SiLU and
-// GeGLU-tanh backward two 16-byte ones, ReGLU one 16-byte access.
+// GeGLU-tanh backward two 16-byte ones, ReGLU one 32-byte access (5-12 % ahead
+// of one 16-byte access on its forward at every width and dtype in alternating
+// runs, level or ahead on its backward).
 struct LaunchDefault {
     int8_t vec_bytes, unroll;
 };
 constexpr LaunchDefault kDefaults[3][4][2] = {
     // f32:  silu            gelu_erf         gelu_tanh        relu
-    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {32, 1}}, {{16, 1}, {16, 1}}},
+    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {32, 1}}, {{32, 1}, {32, 1}}},
     // f16
-    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{16, 2}, {16, 1}}},
+    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{32, 1}, {32, 1}}},
     // bf16
-    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{16, 1}, {16, 1}}},
+    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{32, 1}, {32, 1}}},
 };
 
 constexpr int kMaxDevices = 64;
