@@ -252,7 +252,12 @@ int glu_version(void);
  * when y, its row stride and its row width are 16-byte multiples; else 16 or
  * 2 from registers), grid =
  * blocks of the persistent grid, vector_units = tiles of y, and threads as
- * launched; the other fields are 0. */
+ * launched; the other fields are 0.  For glu_add_rmsnorm_fwd and
+ * glu_add_rmsnorm_bwd: vector_units = rows, unroll = elements per thread and
+ * row, vec_bytes 16 or the element size, and path names the kernel: 4 the
+ * forward, or the backward with element accesses; the backward on 16-byte
+ * rows 6 (rows staged in shared memory), 7 (narrow rows held in registers,
+ * one block per group of rows) or 8 (persistent teams of registers). */
 typedef struct {
     int32_t launched;     /* 1 if a kernel was enqueued */
     int32_t backward;     /* 0 = forward kernel, 1 = backward kernel */
@@ -498,13 +503,15 @@ int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride,
  * GLU_ERR_ALIAS for any other overlap, asynchronous on `stream`).
  *
  * Rows whose operands are 16-byte aligned (bases, strides, width) and whose
- * inputs dy, h, dh and rstd are in device memory are staged in shared memory
- * by the bulk-copy engine, except narrow rows (up to 128 16-byte vectors) in
- * a launch small enough to fit on the GPU at once, which are loaded straight
- * into registers.  Every wait of the staged kernel is bounded (about a
- * second); one that runs out is counted by glu_wait_timeouts() and leaves
- * that launch's outputs and dgamma incomplete.  Other rows (pinned host
- * inputs included) use element accesses.
+ * inputs dy, h, dh and rstd are in device memory use 16-byte accesses: rows of
+ * up to 384 16-byte vectors are loaded straight into registers (narrow rows,
+ * up to 128 vectors, one block per group of rows when the launch fits on the
+ * GPU at once; otherwise a persistent grid of teams of threads, one row per
+ * team at a time), wider rows are staged in shared memory by the bulk-copy
+ * engine.  Every wait of the staged kernel is bounded (about a second); one
+ * that runs out is counted by glu_wait_timeouts() and leaves that launch's
+ * outputs and dgamma incomplete.  Other rows (pinned host inputs included)
+ * use element accesses.
  */
 int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride,
                         const void *h, int64_t h_stride,

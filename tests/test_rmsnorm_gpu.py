@@ -236,13 +236,16 @@ def run_bwd(dy, h, rstd, g, dh, dt, dres=False, dgamma=True):
 
 
 TORCH_INT_OF = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}
-# (30011, 64) and (6000, 1024): stages that go round the shared-memory ring
-# of the 16-byte path several times, the last one ragged; (9, 5000): a
+# (30011, 64) and (6000, 1024): the persistent team kernel with several rows
+# per team; (3001, 6144): stages that go round the shared-memory ring of the
+# staged kernel several times, the last one ragged; (9, 5000): a
 # 160-thread team beside the producer warp; (33, 8200): just past 1024
 # vectors a row (16-bit types), the kernel without a producer warp on a
-# 288-thread team
+# 288-thread team; (5000, 1000): the persistent team kernel with the last
+# vectors of a row past some threads' reach (125 and 250 vectors a row);
+# (64, 4096): 512 vectors (16-bit types), just past the team kernel
 BWD_SHAPES = [(1, 1), (3, 7), (5, 64), (77, 100), (33, 1000), (64, 4096), (9, 5000), (17, 8192), (4, 16384),
-              (513, 1536), (30011, 64), (6000, 1024), (33, 8200)]
+              (513, 1536), (30011, 64), (6000, 1024), (33, 8200), (5000, 1000), (3001, 6144)]
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -257,9 +260,27 @@ def test_bwd_parity(orc, shape, dt):
         V = 16 // E
         vec = (H * E) % 16 == 0 and H <= 2048 * V
         assert info["backward"] == 1 and info["vec_bytes"] == (16 if vec else E) and info["grid"] <= rows
-        # 16-byte rows: the fewest 16-byte accesses per operand per thread (1, 2 or 4) that keep a row
-        # within the 256 consumer threads beside the producer warp; wider rows 4 at 512 threads
-        nv = 1 if H <= 256 * V else 2 if H <= 512 * V else 4
+        nvec = H // V
+        if not vec:
+            assert info["path"] == 4
+            nv = 0
+        elif info["path"] == 7:
+            # the narrow kernel: one 16-byte access per operand per thread and row, rows of up to 128
+            assert nvec <= 128 and info["threads"] == 256
+            nv = 1
+        elif nvec <= 384:
+            # the persistent team kernel: 4 accesses per operand per thread where every lane of a warp
+            # has 4 (at most 2 with dh), else 2 or 1; whole teams of whole warps, at most 1024 threads
+            assert info["path"] == 8
+            nv = 4 if nvec >= 128 else 2 if nvec >= 64 else 1
+            nv = min(nv, 2) if with_dh else nv
+            tpr = (-(-nvec // nv) + 31) // 32 * 32
+            assert info["threads"] % tpr == 0 and info["threads"] <= 1024
+        else:
+            # the staged kernel: the fewest accesses (2 or 4) that keep a row within 256 consumer
+            # threads beside the producer warp; wider rows 4 at 512 threads
+            assert info["path"] == 6
+            nv = 2 if H <= 512 * V else 4
         assert info["unroll"] == (nv * V if vec else 16)
         assert glu.glu_wait_timeouts() == 0
         check_bwd(orc, dt, dy, h, rstd, g, dh, dx, dg, f"bwd {dt} {shape} dh={with_dh}")
