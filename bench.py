@@ -835,7 +835,12 @@ def run_gemm(args):
     fused_ms = timed(fused, K, W, clocks)
     clock_info = clocks.stop()
     info = glu.glu_last_launch()
-    gemm_ms = timed(lambda: torch.matmul(x, w.T, out=h), K, W)
+    # the same clock record for cuBLAS's GEMM: under the power cap the two
+    # kernels can run at different SM clocks, which the ratio of times includes
+    gemm_clocks = ClockSampler(gpu_selector(0))
+    gemm_clocks.start()
+    gemm_ms = timed(lambda: torch.matmul(x, w.T, out=h), K, W, gemm_clocks)
+    gemm_clock_info = gemm_clocks.stop()
     unfused_ms = timed(unfused, K, W)
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     peak = float(peaks["bf16_tflops"])
@@ -856,7 +861,8 @@ def run_gemm(args):
                        "cublas_gemm_ms": round(gemm_ms, 4),
                        "cublas_gemm_tflops": round(flops / (gemm_ms * 1e-3) / 1e12, 1),
                        "cublas_gemm_plus_glu_fwd_ms": round(unfused_ms, 4),
-                       "speedup_vs_unfused": round(unfused_ms / fused_ms, 4)},
+                       "speedup_vs_unfused": round(unfused_ms / fused_ms, 4),
+                       "cublas_gemm_clocks": gemm_clock_info},
         "shapes": shapes,
         "gpu_launches": K,
         "clocks": clock_info,
