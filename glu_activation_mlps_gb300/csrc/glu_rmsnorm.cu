@@ -26,7 +26,8 @@
 // The backward (glu_add_rmsnorm_bwd, below the forward) has four kernels, for
 // 16-byte rows in device memory: add_rmsnorm_bwd_narrow_kernel for narrow rows
 // when its grid fits on the GPU at once, add_rmsnorm_bwd_teams_kernel (a
-// persistent grid of register teams) for other rows of up to 384 vectors, and
+// persistent grid of register teams) for other rows of up to 512 vectors
+// (384 for f32), and
 // add_rmsnorm_bwd_staged_kernel (rows staged in shared memory by the
 // bulk-copy engine) for wider ones; add_rmsnorm_bwd_kernel with element
 // accesses takes the rest.
@@ -52,7 +53,18 @@ struct Params {
     int64_t rows;
     int H;
     float eps;
+    int prefetch;               // 16-byte rows: ask L2 for the block's first row before the dependency wait
 };
+
+// An L2 prefetch of `bytes` bytes at q by the bulk-copy engine (q 16-byte
+// aligned, bytes a multiple of 16).  Used before a kernel waits for the
+// previous grid: L2 is the point of coherence, so a line that grid writes
+// after the prefetch is simply fetched again, and nothing enters the core's
+// own caches before the wait.
+__device__ __forceinline__ void prefetch_bulk(const void *q, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(q), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ float warp_sum(float v)
 {
@@ -119,6 +131,11 @@ __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
     __shared__ float red[2][33];
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the block's first row of x and the residual, asked of L2 before the wait
+    if (VEC && p.prefetch && threadIdx.x == 0 && blockIdx.x < p.rows) {
+        prefetch_bulk(p.x + int64_t(blockIdx.x) * p.sx, uint32_t(p.H) * sizeof(T));
+        prefetch_bulk(p.res + int64_t(blockIdx.x) * p.sr, uint32_t(p.H) * sizeof(T));
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int t = threadIdx.x, nt = blockDim.x;
@@ -242,6 +259,11 @@ __global__ void __launch_bounds__(EPT <= 16 ? 1024 : 512)
     __shared__ float red[2][33];
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the block's first row of x and the residual, asked of L2 before the wait
+    if (p.prefetch && threadIdx.x == 0 && blockIdx.x < p.rows) {
+        prefetch_bulk(p.x + int64_t(blockIdx.x) * p.sx, uint32_t(p.H) * sizeof(T));
+        prefetch_bulk(p.res + int64_t(blockIdx.x) * p.sr, uint32_t(p.H) * sizeof(T));
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int t = threadIdx.x, nt = blockDim.x;
@@ -559,6 +581,18 @@ __global__ void __launch_bounds__(PROD ? kRmsBwdConsumersP + 32 : kRmsBwdThreads
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    // the block's first stage of rows (dy, h and dh), asked of L2 before the wait
+    if (warp == 0) {
+        const int64_t base = int64_t(blockIdx.x) * SR;
+        const int n = base < p.rows ? int(p.rows - base < SR ? p.rows - base : SR) : 0;
+        for (int j = lane; j < n * nin; j += 32) {
+            const int op = j / n, r = j - op * n;
+            const char *src = op == 0   ? p.dy + (base + r) * p.sdy
+                              : op == 1 ? p.h + (base + r) * p.sh
+                                        : p.dh + (base + r) * p.sdh;
+            prefetch_bulk(src, rb);
+        }
+    }
     __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -785,14 +819,22 @@ __global__ void __launch_bounds__(kRmsBwdNarrowThreads, 2)
     __shared__ float dgs[1024];                                   // the teams' dgamma partial sums
     const int TM = p.groups, tpr = p.tpr, nwg = tpr >> 5;
 
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
     const int lane = threadIdx.x & 31;
     const int t = threadIdx.x / tpr, tg = threadIdx.x - t * tpr, wig = tg >> 5;
     const int col = tg * V;
     const bool on_col = t < TM && col < p.H;
     const int64_t row0 = (int64_t(blockIdx.x) * TM + t) * R;
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the team's rows of dy and h, asked of L2 before the wait
+    if (t < TM && tg < R) {
+        const int64_t row = row0 + tg;
+        if (row < p.rows) {
+            prefetch_bulk(p.dy + row * p.sdy, uint32_t(p.H) * sizeof(T));
+            prefetch_bulk(p.h + row * p.sh, uint32_t(p.H) * sizeof(T));
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     uint32_t gw[W] = {0, 0, 0, 0};
     if (on_col) Access<16>::load(p.gamma + int64_t(col) * sizeof(T), gw);
@@ -867,10 +909,10 @@ __global__ void __launch_bounds__(kRmsBwdNarrowThreads, 2)
     add_dgamma<V, 1>(p.dgamma, p.H, TM, dgf, [&](int) { return on_col ? col : 0; }, dgs);
 }
 
-// Rows of up to 384 16-byte vectors (3072 elements of 16-bit types, 1536 of
-// fp32) in device memory, where the staged kernel's ring would hold only a few
-// stages per SM and its fill and drain would decide the time: a persistent grid
-// of register teams.  One block per SM of up to 1024 threads (64 registers
+// Rows of up to 512 16-byte vectors of 16-bit types (4096 elements) or 384 of
+// fp32 (1536 elements) in device memory, where the staged kernel's ring would
+// hold only a few stages per SM and its fill and drain would decide the time:
+// a persistent grid of register teams.  One block per SM of up to 1024 threads (64 registers
 // each) holds G teams of tpr threads.  A team works on one row at a time and a
 // thread on NV 16-byte vectors of it (vector k * tpr + tg), loaded straight
 // into registers before any arithmetic, so an SM keeps up to 1024 x NV x 32
@@ -925,12 +967,28 @@ __global__ void __launch_bounds__(kRmsBwdTeamThreads, 1)
     float *dgs = reinterpret_cast<float *>(team_smem + int64_t(nvec) * 16);
     float *xch = dgs + int64_t(G) * Hp;
 
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
     const int t = threadIdx.x / tpr, tg = threadIdx.x - t * tpr, lane = threadIdx.x & 31, wig = tg >> 5;
     const int64_t step = int64_t(gridDim.x) * G;
     int64_t row = int64_t(t) * gridDim.x + blockIdx.x;
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Before waiting for the previous grid, ask L2 for the team's first row of
+    // dy and h, so that DRAM starts on it during that grid's last blocks.  L2 is
+    // the point of coherence: a line the previous grid writes after the
+    // prefetch is simply fetched again, and nothing is read from the core's
+    // own caches before the wait.
+    if (row < p.rows) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int jv = k * tpr + tg;
+            if (jv < nvec) {
+                const int64_t off = int64_t(jv) * 16;
+                prefetch_line(p.dy + row * p.sdy + off);
+                prefetch_line(p.h + row * p.sh + off);
+            }
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     uint32_t wd[NV][4], ws[NV][4], we[DH ? NV : 1][4];
     float rs = 0.0f;
     // a row's loads, and an L2 prefetch of the team's next row
@@ -1294,6 +1352,13 @@ extern "C" int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride, const void *
     p.rows = n_rows;
     p.H = int(n_cols);
     p.eps = eps;
+    // The L2 prefetch before the dependency wait pays where the blocks resident
+    // at the start cover most rows: the persistent kernel, and launches of at
+    // most 32 MiB of inputs.  With one block per row over several waves, the
+    // later blocks would only prefetch the row they load next (measured: 4096
+    // rows of 4096 bf16 3 % slower with it, 1024 / 2048 columns 4 / 2 % faster,
+    // the persistent kernel at 8192 / 16384 columns 3 / 2 % faster).
+    p.prefetch = vec && (rows_kernel || 2 * n_rows * n_cols * E <= (int64_t(32) << 20));
     KernelFn fn = pick(dtype, ept, vec, rows_kernel);
     int64_t blocks = n_rows;
     if (rows_kernel) {      // persistent: as many blocks as fit on the GPU at once
@@ -1415,15 +1480,17 @@ extern "C" int glu_add_rmsnorm_bwd(const void *dy, int64_t dy_stride, const void
         }
         narrow = (n_rows + narrow_rows - 1) / narrow_rows <= int64_t(resident) * sms;
     }
-    // Rows of up to 384 vectors that the narrow kernel does not take: the
-    // persistent team kernel, with 4 vectors per operand per thread where a
-    // row has at least 4 for every lane of a warp (at most 2 with dh, whose
-    // rows are held as well), else 2 or 1.  (Measured against the staged
-    // kernel at 4096 rows: 1.1-1.4 times faster up to 384 vectors, and at
-    // 65536 rows of 32 vectors twice as fast; 3-10 % slower at 512.)
+    // Rows that the narrow kernel does not take, of up to 512 vectors (16-bit
+    // types) or 384 (f32): the persistent team kernel, with 4 vectors per
+    // operand per thread where a row has at least 4 for every lane of a warp
+    // (at most 2 with dh, whose rows are held as well), else 2 or 1.
+    // (Measured against the staged kernel, both with their first rows asked
+    // of L2 before the dependency wait: 1.1-1.4 times faster at 4096 rows of
+    // 1024-3072 bf16, 1.06 at 4096 and 1.35 at 1024 x 4096, twice as fast at
+    // 65536 rows of 256; 8 % slower at 4096 rows of 2048 f32, 512 vectors.)
     const int64_t nvec = n_cols / V;
     int nvt = 0;
-    if (staged && !narrow && nvec <= 384) {
+    if (staged && !narrow && nvec <= (E == 2 ? 512 : 384)) {
         nvt = nvec >= 128 ? 4 : nvec >= 64 ? 2 : 1;
         if (dh && nvt > 2) nvt = 2;
     }

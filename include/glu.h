@@ -504,7 +504,7 @@ int glu_add_rmsnorm_fwd(const void *x, int64_t x_stride,
  *
  * Rows whose operands are 16-byte aligned (bases, strides, width) and whose
  * inputs dy, h, dh and rstd are in device memory use 16-byte accesses: rows of
- * up to 384 16-byte vectors are loaded straight into registers (narrow rows,
+ * up to 512 16-byte vectors (384 for f32) are loaded straight into registers (narrow rows,
  * up to 128 vectors, one block per group of rows when the launch fits on the
  * GPU at once; otherwise a persistent grid of teams of threads, one row per
  * team at a time), wider rows are staged in shared memory by the bulk-copy

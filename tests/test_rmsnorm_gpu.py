@@ -243,7 +243,8 @@ TORCH_INT_OF = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}
 # vectors a row (16-bit types), the kernel without a producer warp on a
 # 288-thread team; (5000, 1000): the persistent team kernel with the last
 # vectors of a row past some threads' reach (125 and 250 vectors a row);
-# (64, 4096): 512 vectors (16-bit types), just past the team kernel
+# (64, 4096): 512 vectors, the widest rows of the team kernel for 16-bit
+# types and past it for f32
 BWD_SHAPES = [(1, 1), (3, 7), (5, 64), (77, 100), (33, 1000), (64, 4096), (9, 5000), (17, 8192), (4, 16384),
               (513, 1536), (30011, 64), (6000, 1024), (33, 8200), (5000, 1000), (3001, 6144)]
 
@@ -268,7 +269,7 @@ def test_bwd_parity(orc, shape, dt):
             # the narrow kernel: one 16-byte access per operand per thread and row, rows of up to 128
             assert nvec <= 128 and info["threads"] == 256
             nv = 1
-        elif nvec <= 384:
+        elif nvec <= (512 if E == 2 else 384):
             # the persistent team kernel: 4 accesses per operand per thread where every lane of a warp
             # has 4 (at most 2 with dh), else 2 or 1; whole teams of whole warps, at most 1024 threads
             assert info["path"] == 8
