@@ -148,6 +148,32 @@ int sm_count()
     return c;
 }
 
+// Blocks of glu::kThreads threads of kernel `fn` resident on one SM at once,
+// asked once per device and kernel variant (`key` < 216: dtype, activation,
+// direction, access width, accesses in flight); 0 if the query fails.
+// Devices numbered 64 and above are asked on every call.
+std::atomic<int> g_resident[kMaxDevices][216];
+
+int resident_blocks(const void *fn, int key)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int c = g_resident[dev][key].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int per = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, glu::kThreads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < kMaxDevices && per > 0) g_resident[dev][key].store(per, std::memory_order_relaxed);
+    return per;
+}
+
 using glu::cuda_fail;
 
 using glu::Call;
@@ -359,6 +385,20 @@ int plan_direct(const Call &c, cudaStream_t stream)
         if (blocks > int64_t(per_sm) * sms) blocks = int64_t(per_sm) * sms;
     }
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    // Forward launches of at most 16 MiB of inputs and more blocks than SMs:
+    // the blocks of the first wave also prefetch the tile one wave ahead
+    // (glu_kernels.cuh).  Measured back to back against the same build without
+    // it (interleaved): 4096 x 1024 bf16 SiLU / GeGLU-erf / ReGLU forward and
+    // 2048 x 2048 SiLU 3-5 % faster; on the backward and on 32-48 MiB
+    // forwards it was up to 7 % slower.
+    if (p.prefetch && c.dir == glu::kFwd && int64_t(2) * c.rows * c.cols * E <= (int64_t(16) << 20)) {
+        const int sms = sm_count();
+        if (sms > 0 && blocks > sms) {
+            const int key = (((c.dtype * 4 + c.act) * 2 + c.dir) * 3 + vb_sel) * 3 + unroll_sel;
+            const int per = resident_blocks(reinterpret_cast<const void *>(fn), key);
+            if (per > 0) p.prefetch_ahead = per * sms;
+        }
+    }
 
     // Launch with a programmatic dependency on the previous kernel in the
     // stream (unless switched off): the kernel waits for that grid itself, so

@@ -241,19 +241,22 @@ __device__ __forceinline__ void bwd_word(uint32_t wa, uint32_t wb, uint32_t wc, 
 
 // ---------------------------------------------------------------- L2 prefetch
 // One prefetch per 128-byte line of this block's first tile of inputs (the
-// lane whose unit holds the line's start).  L2 is the device's point of
-// coherence, so a line the previous grid writes after the prefetch is
-// updated there, and loads issued after griddepcontrol.wait still see its
-// data: the prefetch only lets DRAM start on this launch's inputs during the
-// previous launch's last wave.  Not inlined, so that its address arithmetic
-// does not stay live into the kernel's main loop (inlined, it cost the
-// forward kernel a block per SM).
+// lane whose unit holds the line's start), and with p.prefetch_ahead = the
+// blocks resident at once, of the tile one wave ahead too, which a block of
+// the second wave would otherwise only ask for once it starts.  L2 is the
+// device's point of coherence, so a line the previous grid writes after the
+// prefetch is updated there, and loads issued after griddepcontrol.wait still
+// see its data: the prefetch only lets DRAM start on this launch's inputs
+// during the previous launch's last wave.  Not inlined, so that its address
+// arithmetic does not stay live into the kernel's main loop (inlined, it cost
+// the forward kernel a block per SM).
 template <int VB, int UNROLL, int DIR>
 __device__ __noinline__ void prefetch_first_tile(const Params &p)
 {
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-        const int64_t u = int64_t(blockIdx.x) * kThreads * UNROLL + k * kThreads + threadIdx.x;
+    const int n = p.prefetch_ahead > 0 ? 2 * UNROLL : UNROLL;
+    for (int k = 0; k < n; ++k) {
+        const int64_t tb = int64_t(blockIdx.x) + (k >= UNROLL ? int64_t(p.prefetch_ahead) : 0);
+        const int64_t u = tb * kThreads * UNROLL + (k % UNROLL) * kThreads + threadIdx.x;
         if (u >= p.units) continue;
         int64_t row, cb;
         unit_pos<VB>(p, u, row, cb);

@@ -28,7 +28,7 @@ struct Params {
     uint32_t tail_magic;          // tail index -> (row, element-in-tail)
     uint32_t tail_shift;
     int32_t tail_wide;            // tail_units >= 2^32: plain 64-bit division
-    int32_t pad2;
+    int32_t prefetch_ahead;       // > 0: with the prefetch, also the tile this many blocks ahead
 };
 
 // Unsigned 32-bit division by a runtime-invariant divisor d >= 1 with one
