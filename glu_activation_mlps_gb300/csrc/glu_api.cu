@@ -32,20 +32,23 @@ constexpr int32_t kDefaultCtasPerSm = -1;     // one block per tile
 // Default access width (bytes) and accesses in flight per operand per thread,
 // by [dtype][activation][direction], from a sweep on GB300 of 4096 x {4096,
 // 16384} matrices launched back to back: the forward of the heavier GELUs wants
-// two 32-byte accesses in flight (more arithmetic to hide), the SiLU and
-// GeGLU-tanh backward two 16-byte ones, ReGLU one 32-byte access (5-12 % ahead
-// of one 16-byte access on its forward at every width and dtype in alternating
-// runs, level or ahead on its backward).
+// two 32-byte accesses in flight (more arithmetic to hide), the 16-bit SiLU,
+// GeGLU-erf and GeGLU-tanh backward two 16-byte ones, ReGLU one 32-byte access
+// (5-12 % ahead of one 16-byte access on its forward at every width and dtype in
+// alternating runs, level or ahead on its backward).  Re-swept at 4096 x {1024
+// ... 16384}: the 16-bit GeGLU-erf backward 7-9 % faster with two 16-byte
+// accesses than with one 32-byte access at every width; the f32 SiLU backward
+// 5 % faster at 1024 with one 32-byte access, level (within 0.6 %) above.
 struct LaunchDefault {
     int8_t vec_bytes, unroll;
 };
 constexpr LaunchDefault kDefaults[3][4][2] = {
     // f32:  silu            gelu_erf         gelu_tanh        relu
-    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {32, 1}}, {{32, 1}, {32, 1}}},
+    {{{32, 1}, {32, 1}}, {{32, 2}, {32, 1}}, {{32, 2}, {32, 1}}, {{32, 1}, {32, 1}}},
     // f16
-    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{32, 1}, {32, 1}}},
+    {{{32, 1}, {16, 2}}, {{32, 2}, {16, 2}}, {{32, 2}, {16, 2}}, {{32, 1}, {32, 1}}},
     // bf16
-    {{{32, 1}, {16, 2}}, {{32, 2}, {32, 1}}, {{32, 2}, {16, 2}}, {{32, 1}, {32, 1}}},
+    {{{32, 1}, {16, 2}}, {{32, 2}, {16, 2}}, {{32, 2}, {16, 2}}, {{32, 1}, {32, 1}}},
 };
 
 constexpr int kMaxDevices = 64;
