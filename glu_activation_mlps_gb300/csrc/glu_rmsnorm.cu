@@ -912,20 +912,25 @@ __global__ void __launch_bounds__(kRmsBwdNarrowThreads, 2)
 // Rows of up to 512 16-byte vectors of 16-bit types (4096 elements) or 384 of
 // fp32 (1536 elements) in device memory, where the staged kernel's ring would
 // hold only a few stages per SM and its fill and drain would decide the time:
-// a persistent grid of register teams.  One block per SM of up to 1024 threads (64 registers
-// each) holds G teams of tpr threads.  A team works on one row at a time and a
-// thread on NV 16-byte vectors of it (vector k * tpr + tg), loaded straight
-// into registers before any arithmetic, so an SM keeps up to 1024 x NV x 32
-// bytes of dy and h in flight.  Rows go to the teams round robin over the
-// blocks (row (i * G + t) * grid + block), which spreads them evenly over the
-// SMs.  gamma sits in shared memory.  Each team adds its dgamma partial sums
-// to a private fp32 row in shared memory (each element read, added and written
-// back by the thread that owns its column; the two halves of a 16-bit vector's
-// eight columns lie in two half-rows, so a warp's 16-byte accesses do not
-// collide in the banks), and the block adds the sum of its teams' rows to
-// dgamma once at the end.  A team of several warps shares its warp sums
-// through shared memory under its own named barrier (at most 15 teams then);
-// consecutive rows alternate between two exchange arrays, as in group_sum.
+// a persistent grid of register teams.
+//   - One block per SM of up to 1024 threads (64 registers each) holds G teams
+//     of tpr threads.  A team works on one row at a time and a thread on NV
+//     16-byte vectors of it (vector k * tpr + tg), loaded straight into
+//     registers before any arithmetic, so an SM keeps up to 1024 x NV x 32
+//     bytes of dy and h in flight.
+//   - Rows go to the teams round robin over the blocks (row (i * G + t) * grid
+//     + block), which spreads them evenly over the SMs.  Before waiting for the
+//     previous grid a team asks L2 for its first row; each row's loads come with
+//     an L2 prefetch of the team's next row.
+//   - gamma sits in shared memory.  Each team adds its dgamma partial sums to a
+//     private fp32 row in shared memory (each element read, added and written
+//     back by the thread that owns its column; the two halves of a 16-bit
+//     vector's eight columns lie in two half-rows, so a warp's 16-byte accesses
+//     do not collide in the banks), and the block adds the sum of its teams'
+//     rows to dgamma once at the end.
+//   - A team of several warps shares its warp sums through shared memory under
+//     its own named barrier (at most 15 teams then); consecutive rows alternate
+//     between two exchange arrays, as in group_sum.
 constexpr int kRmsBwdTeamThreads = 1024;
 
 // The team kernel's final dgamma sum: P threads per group of four columns
